@@ -1,0 +1,359 @@
+"""Benchmark: NVFP4 linear-layer step (Fprop + Dgrad + Wgrad) on GB300.
+
+Workload: the MLP up-projection layer, M=8192 tokens, K=5120, N=20480, BF16
+inputs drawn by nvfp4_bit_numerics_gb300.workloads (X ~ N(0,1) with 8 outlier
+channels x30, W ~ N(0, 0.014), dY ~ N(0, 1e-4)).  One step = every part of
+the path: amax (plain and Hadamard-transformed), X -> rowwise + transposed
+Hadamard quantization, W -> 2D 16x16 quantization (W and W^T), dY ->
+rowwise + transposed Hadamard quantization with stochastic rounding, and
+the three block-scaled FP4 GEMMs.  Throughput = 6*M*K*N flops per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  Under torchrun every rank runs its own layer step on
+its own token shard (weak scaling; data-parallel ranks need no exchange on
+this path); rank 0 prints.  --impl reference times the CPU oracle on a
+64-token slice of the same layer step.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, K, N = 8192, 5120, 20480
+FLOPS_PER_STEP = 6 * M * K * N          # three GEMMs of 2*M*N*K
+FLOPS_PER_GEMM = 2 * M * K * N
+WORKLOAD = "nvfp4_linear_fwd_bwd_mlp_up_8192x5120x20480"
+SEED = 2
+ORACLE_TOKENS = 64
+FP4_OVER_BF16 = 13.5 / 2.25             # nominal dense FP4 : BF16 tensor-core ratio
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", HBM_FALLBACK_GBS), d.get("bf16_tflops", BF16_FALLBACK_TFLOPS), "measured"
+    return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record():
+    """DRAM bytes per GEMM launch from the committed ncu summary, valid only
+    while the GEMM source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    src = os.path.join(ROOT, "nvfp4_bit_numerics_gb300", "csrc", "gemm_kernel.cu")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    if rec.get("gemm_kernel_sha256") != h:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def cpu_oracle_step(x_f, w_f, dy_f):
+    """One bounded oracle sample: the whole layer step for a 64-token slice of
+    X and dY (all of W).  Returns (seconds, flops)."""
+    from oracle import linear
+
+    xs, dys = x_f[:ORACLE_TOKENS], dy_f[:ORACLE_TOKENS]
+    t0 = time.perf_counter()
+    f = linear.linear_fwd(xs, w_f, SEED)
+    linear.linear_bwd(dys, f, SEED)
+    return time.perf_counter() - t0, 6 * ORACLE_TOKENS * K * N
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+    from nvfp4_bit_numerics_gb300 import workloads
+
+    x, w, dy = workloads.mlp_up()
+    x_f, w_f, dy_f = (workloads.bf16_to_f32_numpy(t) for t in (x, w, dy))
+    for _ in range(args.warmup):
+        cpu_oracle_step(x_f, w_f, dy_f)
+    times = []
+    flops = 0
+    for _ in range(args.steps):
+        dt, fl = cpu_oracle_step(x_f, w_f, dy_f)
+        times.append(dt)
+        flops = fl
+    mean = sum(times) / len(times)
+    value = flops / mean / 1e12
+    cores = os.cpu_count()
+    sample = "%d-token slice of the layer step (all of W), %.1f GFLOP per step" % (ORACLE_TOKENS, flops / 1e9)
+    line = {
+        "impl": "reference", "metric": "NVFP4 linear fwd+bwd TFLOPS", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "sample_tokens": ORACLE_TOKENS},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from nvfp4_bit_numerics_gb300 import binding as B
+    from nvfp4_bit_numerics_gb300 import build as nbuild
+    from nvfp4_bit_numerics_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    nbuild.build()
+    B.load_library()
+
+    # each rank draws its own token shard (weak scaling)
+    x_h, w_h, dy_h = workloads.mlp_up(seed=SEED + 1000 * rank)
+    x, w, dy = x_h.to(dev), w_h.to(dev), dy_h.to(dev)
+    ws = B.linear_workspace(M, K, N, device=dev)
+    v = B.nvfp4_linear_get_views(ws, M, K, N)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(marks=None):
+        # the launches of nvfp4_linear_fwd / nvfp4_linear_bwd, issued through
+        # the public primitives so that events can bracket each part
+        def mark(i):
+            if marks is not None:
+                marks[i].record(stream)
+        mark(0)
+        B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, B.NVFP4_ROUND_RNE, rht=True, seed=SEED,
+                         out=v["xq"], out_t=v["xtq"])
+        mark(1)
+        B.nvfp4_quantize(w, B.NVFP4_Q_2D, out=v["wq"], out_t=v["wtq"])
+        mark(2)
+        B.nvfp4_gemm(v["xq"], v["wq"], out=y)
+        mark(3)
+        B.nvfp4_quantize(dy, B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, B.NVFP4_ROUND_SR, rht=True, seed=SEED, sr_stream=0,
+                         sr_stream_t=1, out=v["dyq"], out_t=v["dytq"])
+        mark(4)
+        B.nvfp4_gemm(v["dyq"], v["wtq"], out=dx)
+        mark(5)
+        B.nvfp4_gemm(v["dytq"], v["xtq"], out=dw)
+        mark(6)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    if B.nvfp4_get_status() != B.NVFP4_OK:
+        raise RuntimeError("device status after warm-up")
+
+    marks = [[ev() for _ in range(7)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = B.nvfp4_kernel_launch_count()
+    t_start, t_end = ev(), ev()
+    barrier()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(marks[i])
+    t_end.record(stream)
+    barrier()
+    launches = B.nvfp4_kernel_launch_count() - launches0
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    st = B.nvfp4_get_status()
+    if st != B.NVFP4_OK:
+        raise RuntimeError("device status %d in the timed region" % st)
+
+    part = np.array([[marks[i][j].elapsed_time(marks[i][j + 1]) for j in range(6)] for i in range(args.steps)])
+    gemm_ms = float(np.mean(part[:, [2, 4, 5]]))
+    ms_per_step = total_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    # e2e: the public layer API on pinned host buffers, copies inside the region
+    xp, wp, dyp = (t.pin_memory() for t in (x_h, w_h, dy_h))
+    yp = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    dxp = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    dwp = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        x.copy_(xp, non_blocking=True)
+        w.copy_(wp, non_blocking=True)
+        dy.copy_(dyp, non_blocking=True)
+        B.nvfp4_linear_fwd(x, w, SEED, ws, y=y)
+        B.nvfp4_linear_bwd(dy, K, SEED, ws, dx=dx, dw=dw)
+        yp.copy_(y, non_blocking=True)
+        dxp.copy_(dx, non_blocking=True)
+        dwp.copy_(dw, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    e0, e1 = ev(), ev()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (x_h, w_h, dy_h))
+    d2h = sum(t.numel() * t.element_size() for t in (yp, dxp, dwp))
+
+    if rank != 0:
+        return 0
+    hbm, bf16, src = measured_peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16
+    achieved = FLOPS_PER_GEMM / (gemm_ms * 1e-3) / 1e12
+    # quantize GB/s of the dY pass (algorithmic: two reads of dY for amax and
+    # quantize, two NVFP4 outputs of 0.5625 B per element each)
+    dy_elems = M * N
+    q_bytes = dy_elems * (2 + 2 + 2 * 0.5625)
+    q_ms = float(np.mean(part[:, 3]))
+    cpu_s, cpu_flops = cpu_oracle_step(*(workloads.bf16_to_f32_numpy(t) for t in (x_h, w_h, dy_h)))
+    value = FLOPS_PER_STEP * world / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": "NVFP4 linear fwd+bwd TFLOPS", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "parallelism": "dp%d" % world,
+                   "l2": "inputs larger than L2 (X+W+dY = 629 MB read per step)",
+                   "pct_fp4_peak": 100.0 * value / world / fp4_peak},
+        "parts_ms": {"quant_x": float(np.mean(part[:, 0])), "quant_w2d": float(np.mean(part[:, 1])),
+                     "gemm_fprop": float(np.mean(part[:, 2])), "quant_dy": q_ms,
+                     "gemm_dgrad": float(np.mean(part[:, 4])), "gemm_wgrad": float(np.mean(part[:, 5]))},
+        "quantize_gbs": {"dy_fused_sr_rht": q_bytes / (q_ms * 1e-3) / 1e9, "unit": "GB/s",
+                         "bytes": "2 reads of BF16 dY (amax, quantize) + 2 x 0.5625 B/elem written"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp4_peak, "traffic": traffic_record(),
+                     "kernel": "nvfp4_gemm_kernel<256> (mean of Fprop, Dgrad, Wgrad)",
+                     "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:BF16)" % (src, bf16,
+                                                                                         FP4_OVER_BF16)},
+        "e2e": {"value": FLOPS_PER_STEP * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "api": "nvfp4_linear_fwd + nvfp4_linear_bwd"},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "cpu_baseline": {"value": cpu_flops / cpu_s / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": "%d-token slice of the layer step (all of W); numpy elementwise on one "
+                                   "thread, float64 BLAS GEMM on the host's cores" % ORACLE_TOKENS},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gpu":
+        args.warmup = 3
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,304 @@
+// api.cu -- the C ABI declared in include/nvfp4.h: argument validation, the
+// per-device status word, the linear-layer workspace layout and the Fprop /
+// Dgrad / Wgrad orchestration.
+//
+// Method: "Pretraining Large Language Models with NVFP4" (gist.science
+// summary), Resumo técnico §2 Metodologia.  One layer step enqueues, on the
+// caller's stream:
+//   fwd: amax(X) and amax(Hadamard(X^T)) in one read; amax(W);
+//        X -> {X rowwise RNE, X^T Hadamard RNE} in one read;
+//        W -> {W, W^T} with 16x16 blocks (item 3);
+//        Y = X W^T on the tensor cores.
+//   bwd: amax(dY) and amax(Hadamard(dY^T)) in one read;
+//        dY -> {dY rowwise SR, dY^T Hadamard SR} in one read (items 2, 4);
+//        dX = dY W and dW = dY^T X on the tensor cores.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+
+#include "internal.h"
+
+namespace nvfp4 {
+
+std::atomic<uint64_t> g_launches{0};
+
+namespace {
+
+__device__ uint32_t g_status_word;
+
+uint32_t* g_status_ptr[64] = {nullptr};
+
+// Random stream ids of one layer step (Philox key = the step's seed).
+constexpr uint32_t kStreamDy = 0;   // stochastic rounding of dY (Dgrad operand)
+constexpr uint32_t kStreamDyT = 1;  // stochastic rounding of dY^T (Wgrad operand)
+
+nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+bool valid_tensor(const nvfp4_tensor* t) {
+  return t && t->codes && t->scales && t->tensor_scale && aligned16(t->codes) && aligned16(t->scales) &&
+         (t->scale_layout == NVFP4_SCALES_LINEAR || t->scale_layout == NVFP4_SCALES_MMA);
+}
+
+bool layout_ok(const nvfp4_tensor* t) {
+  if (t->scale_layout == NVFP4_SCALES_MMA) return t->rows % 128 == 0 && t->cols % 64 == 0;
+  return true;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+uint32_t* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_ARG: return "invalid argument";
+    case NVFP4_ERR_SHAPE: return "invalid shape";
+    case NVFP4_ERR_ALIGN: return "misaligned pointer or pitch";
+    case NVFP4_ERR_NONFINITE: return "non-finite amax";
+    case NVFP4_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case NVFP4_ERR_CUDA: return "CUDA runtime error";
+    case NVFP4_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+uint64_t nvfp4_kernel_launch_count(void) { return g_launches.load(); }
+
+nvfp4_status nvfp4_get_status(nvfp4_stream stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_status_word, sizeof(w)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (w) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+  if (w & kStatusTimeout) return NVFP4_ERR_TIMEOUT;
+  if (w & kStatusNonFinite) return NVFP4_ERR_NONFINITE;
+  return NVFP4_OK;
+}
+
+size_t nvfp4_scale_bytes(int64_t rows, int64_t cols, int32_t layout) {
+  if (rows < 0 || cols < 0) return 0;
+  const int64_t nkb = cols / 16;
+  if (layout == NVFP4_SCALES_MMA) return (size_t)(((rows + 127) / 128) * ((nkb + 3) / 4) * 512);
+  return (size_t)(rows * nkb);
+}
+
+nvfp4_status nvfp4_amax(const void* x, int64_t rows, int64_t cols, int32_t flags, uint64_t rht_seed,
+                        float* amax_dev, nvfp4_stream stream) {
+  if (!amax_dev || (flags & ~7) || !flags) return NVFP4_ERR_ARG;
+  if (rows < 0 || cols < 0 || cols % 16) return NVFP4_ERR_SHAPE;
+  if ((flags & NVFP4_AMAX_RHT_COLS) && rows % 16) return NVFP4_ERR_SHAPE;
+  if (rows * cols > 0 && (!x || !aligned16(x))) return x ? NVFP4_ERR_ALIGN : NVFP4_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(amax_dev) & 3u) != 0) return NVFP4_ERR_ALIGN;
+  return from_cuda(launch_amax(x, rows, cols, (flags & NVFP4_AMAX_PLAIN) ? amax_dev : nullptr,
+                               (flags & NVFP4_AMAX_RHT_ROWS) ? amax_dev + 1 : nullptr,
+                               (flags & NVFP4_AMAX_RHT_COLS) ? amax_dev + 2 : nullptr, rht_seed,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, const nvfp4_quant_cfg* cfg,
+                            const nvfp4_tensor* out, const nvfp4_tensor* out_t, nvfp4_stream stream) {
+  if (!cfg || !x) return NVFP4_ERR_ARG;
+  if (cfg->kind < NVFP4_Q_ROWWISE || cfg->kind > NVFP4_Q_2D) return NVFP4_ERR_ARG;
+  if (cfg->rounding != NVFP4_ROUND_RNE && cfg->rounding != NVFP4_ROUND_SR) return NVFP4_ERR_ARG;
+  if (rows <= 0 || cols <= 0 || rows % 64 || cols % 64) return NVFP4_ERR_SHAPE;
+  if (!aligned16(x)) return NVFP4_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool sr = cfg->rounding == NVFP4_ROUND_SR;
+  const bool rht = cfg->rht != 0;
+  const nvfp4_tensor* o_row = nullptr;
+  const nvfp4_tensor* o_t = nullptr;
+  switch (cfg->kind) {
+    case NVFP4_Q_ROWWISE: o_row = out; break;
+    case NVFP4_Q_TRANSPOSE: o_t = out; break;
+    case NVFP4_Q_ROWWISE_AND_TRANSPOSE: o_row = out; o_t = out_t; break;
+    case NVFP4_Q_2D: o_row = out; o_t = out_t; break;
+  }
+  if (!o_row && !o_t) return NVFP4_ERR_ARG;
+  if (cfg->kind == NVFP4_Q_ROWWISE_AND_TRANSPOSE && !o_t) return NVFP4_ERR_ARG;
+  for (const nvfp4_tensor* t : {o_row, o_t}) {
+    if (!t) continue;
+    if (!valid_tensor(t) || !t->amax) return NVFP4_ERR_ARG;
+    if (!layout_ok(t)) return NVFP4_ERR_SHAPE;
+  }
+  if (o_row && (o_row->rows != rows || o_row->cols != cols)) return NVFP4_ERR_SHAPE;
+  if (o_t && (o_t->rows != cols || o_t->cols != rows)) return NVFP4_ERR_SHAPE;
+
+  cudaError_t e = cudaSuccess;
+  if (cfg->kind == NVFP4_Q_2D) {
+    if (cfg->compute_amax) {
+      e = launch_amax(x, rows, cols, o_row->amax, nullptr, nullptr, 0, s);
+      // the W^T output shares W's amax
+      if (e == cudaSuccess && o_t && o_t->amax != o_row->amax)
+        e = cudaMemcpyAsync(o_t->amax, o_row->amax, sizeof(float), cudaMemcpyDeviceToDevice, s);
+      if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    }
+    return from_cuda(launch_quant_2d(x, rows, cols, *o_row, o_t, o_row->amax, s));
+  }
+
+  if (cfg->compute_amax) {
+    float* a_row = o_row ? o_row->amax : nullptr;
+    float* a_t = o_t ? o_t->amax : nullptr;
+    if (cfg->kind == NVFP4_Q_ROWWISE) {
+      e = rht ? launch_amax(x, rows, cols, nullptr, a_row, nullptr, cfg->seed, s)
+              : launch_amax(x, rows, cols, a_row, nullptr, nullptr, 0, s);
+    } else if (rht) {
+      // one read gives max|x| (rowwise output) and max|Q x| along rows
+      e = launch_amax(x, rows, cols, a_row, nullptr, a_t, cfg->seed, s);
+    } else {
+      e = launch_amax(x, rows, cols, a_t, nullptr, nullptr, 0, s);
+      if (e == cudaSuccess && a_row && a_row != a_t)
+        e = cudaMemcpyAsync(a_row, a_t, sizeof(float), cudaMemcpyDeviceToDevice, s);
+    }
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+  if (cfg->kind == NVFP4_Q_ROWWISE)
+    return from_cuda(launch_quant_rowwise(x, rows, cols, *o_row, o_row->amax, rht, sr, cfg->seed, cfg->sr_stream, s));
+  // `out` takes sr_stream; the transposed output of the fused kind takes sr_stream_t
+  const uint32_t stream_t = cfg->kind == NVFP4_Q_TRANSPOSE ? cfg->sr_stream : cfg->sr_stream_t;
+  return from_cuda(launch_quant_tile(x, rows, cols, o_row, o_row ? o_row->amax : nullptr, o_t, o_t->amax, rht, sr,
+                                     cfg->seed, cfg->sr_stream, stream_t, s));
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int32_t d_dtype, int64_t ldd,
+                        nvfp4_stream stream) {
+  if (!valid_tensor(a) || !valid_tensor(b) || !d) return NVFP4_ERR_ARG;
+  if (d_dtype != NVFP4_OUT_BF16 && d_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
+  if (a->scale_layout != NVFP4_SCALES_MMA || b->scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_ARG;
+  const int64_t M = a->rows, N = b->rows, K = a->cols;
+  if (M <= 0 || N <= 0 || K <= 0 || b->cols != K) return NVFP4_ERR_SHAPE;
+  if (M % 128 || N % 128 || K % 64 || ldd < N) return NVFP4_ERR_SHAPE;
+  if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return NVFP4_ERR_SHAPE;
+  const int64_t esz = d_dtype == NVFP4_OUT_F32 ? 4 : 2;
+  if (!aligned16(d) || (ldd * esz) % 16) return NVFP4_ERR_ALIGN;
+  return launch_gemm(*a, *b, d, d_dtype, ldd, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Linear layer
+// ---------------------------------------------------------------------------
+// Workspace: a 256-byte header of FP32 scalars, then six NVFP4 tensors, each
+// region 256-byte aligned.  Header floats:
+//   [0] amax X      [2] amax Q(X^T)   [3] amax W (shared by W and W^T)
+//   [4] amax dY     [6] amax Q(dY^T)
+//   [8..13] tensor scales of xq, wq, wtq, xtq, dyq, dytq
+namespace {
+
+struct WsLayout {
+  size_t off_codes[6], off_scales[6], total;
+  int64_t rows[6], cols[6];
+};
+
+WsLayout ws_layout(int64_t M, int64_t K, int64_t N) {
+  WsLayout L{};
+  const int64_t r[6] = {M, N, K, K, M, N};
+  const int64_t c[6] = {K, K, N, M, N, M};
+  size_t off = 256;
+  for (int i = 0; i < 6; ++i) {
+    L.rows[i] = r[i];
+    L.cols[i] = c[i];
+    L.off_codes[i] = off;
+    off = align256(off + (size_t)(r[i] * c[i] / 2));
+    L.off_scales[i] = off;
+    off = align256(off + nvfp4_scale_bytes(r[i], c[i], NVFP4_SCALES_MMA));
+  }
+  L.total = off;
+  return L;
+}
+
+void fill_views(uint8_t* ws, int64_t M, int64_t K, int64_t N, nvfp4_linear_views* v) {
+  const WsLayout L = ws_layout(M, K, N);
+  float* hdr = reinterpret_cast<float*>(ws);
+  float* amax_of[6] = {hdr + 0, hdr + 3, hdr + 3, hdr + 2, hdr + 4, hdr + 6};
+  nvfp4_tensor* t[6] = {&v->xq, &v->wq, &v->wtq, &v->xtq, &v->dyq, &v->dytq};
+  for (int i = 0; i < 6; ++i) {
+    t[i]->codes = ws + L.off_codes[i];
+    t[i]->scales = ws + L.off_scales[i];
+    t[i]->amax = amax_of[i];
+    t[i]->tensor_scale = hdr + 8 + i;
+    t[i]->rows = L.rows[i];
+    t[i]->cols = L.cols[i];
+    t[i]->scale_layout = NVFP4_SCALES_MMA;
+    t[i]->reserved = 0;
+  }
+}
+
+nvfp4_status check_linear(int64_t M, int64_t K, int64_t N, void* ws, size_t ws_bytes) {
+  if (!ws) return NVFP4_ERR_ARG;
+  if (M <= 0 || K <= 0 || N <= 0 || M % 128 || K % 128 || N % 128) return NVFP4_ERR_SHAPE;
+  if (!aligned16(ws)) return NVFP4_ERR_ALIGN;
+  if (ws_bytes < ws_layout(M, K, N).total) return NVFP4_ERR_WORKSPACE;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  if (M <= 0 || K <= 0 || N <= 0) return 0;
+  return ws_layout(M, K, N).total;
+}
+
+nvfp4_status nvfp4_linear_get_views(void* ws, int64_t M, int64_t K, int64_t N, nvfp4_linear_views* views) {
+  if (!ws || !views) return NVFP4_ERR_ARG;
+  if (M <= 0 || K <= 0 || N <= 0 || M % 128 || K % 128 || N % 128) return NVFP4_ERR_SHAPE;
+  fill_views(static_cast<uint8_t*>(ws), M, K, N, views);
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_linear_fwd(const void* x, const void* w, int64_t M, int64_t K, int64_t N, uint64_t seed, void* y,
+                              void* ws, size_t ws_bytes, nvfp4_stream stream) {
+  nvfp4_status st = check_linear(M, K, N, ws, ws_bytes);
+  if (st != NVFP4_OK) return st;
+  if (!x || !w || !y) return NVFP4_ERR_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return NVFP4_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  nvfp4_linear_views v;
+  fill_views(static_cast<uint8_t*>(ws), M, K, N, &v);
+  cudaError_t e = launch_amax(x, M, K, v.xq.amax, nullptr, v.xtq.amax, seed, s);
+  if (e == cudaSuccess) e = launch_amax(w, N, K, v.wq.amax, nullptr, nullptr, 0, s);
+  if (e == cudaSuccess)
+    e = launch_quant_tile(x, M, K, &v.xq, v.xq.amax, &v.xtq, v.xtq.amax, true, false, seed, 0, 0, s);
+  if (e == cudaSuccess) e = launch_quant_2d(w, N, K, v.wq, &v.wtq, v.wq.amax, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  return launch_gemm(v.xq, v.wq, y, NVFP4_OUT_BF16, N, s);
+}
+
+nvfp4_status nvfp4_linear_bwd(const void* dy, int64_t M, int64_t K, int64_t N, uint64_t seed, void* dx, void* dw,
+                              void* ws, size_t ws_bytes, nvfp4_stream stream) {
+  nvfp4_status st = check_linear(M, K, N, ws, ws_bytes);
+  if (st != NVFP4_OK) return st;
+  if (!dy || !dx || !dw) return NVFP4_ERR_ARG;
+  if (!aligned16(dy) || !aligned16(dx) || !aligned16(dw)) return NVFP4_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  nvfp4_linear_views v;
+  fill_views(static_cast<uint8_t*>(ws), M, K, N, &v);
+  cudaError_t e = launch_amax(dy, M, N, v.dyq.amax, nullptr, v.dytq.amax, seed, s);
+  if (e == cudaSuccess)
+    e = launch_quant_tile(dy, M, N, &v.dyq, v.dyq.amax, &v.dytq, v.dytq.amax, true, true, seed, kStreamDy,
+                          kStreamDyT, s);
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  st = launch_gemm(v.dyq, v.wtq, dx, NVFP4_OUT_BF16, K, s);
+  if (st != NVFP4_OK) return st;
+  return launch_gemm(v.dytq, v.xtq, dw, NVFP4_OUT_BF16, K, s);
+}
+
+}  // extern "C"

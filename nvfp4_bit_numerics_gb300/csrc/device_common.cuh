@@ -1,0 +1,219 @@
+// device_common.cuh -- NVFP4 device primitives for sm_103a.
+//
+// Number formats, the two-level scale, the 16-point Hadamard transform and
+// Philox4x32-10, as used by the quantize kernels.  Method: "Pretraining Large
+// Language Models with NVFP4" (gist.science summary), Resumo técnico §2
+// Metodologia (NVFP4 format, two-level scaling, random Hadamard transform,
+// 2D weight blocks, stochastic rounding).  Bit layouts: OCP Microscaling
+// Formats v1.0 (E2M1) and OCP 8-bit Floating Point (E4M3).
+//
+// Every float operation of the scale chain is an explicit IEEE
+// round-to-nearest-even intrinsic (__fmul_rn, __fdiv_rn, __fadd_rn), so the
+// results do not depend on FMA contraction or fast-math flags.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp8.h>
+
+namespace nvfp4 {
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------------------
+// BF16 unpacking: a 16-byte vector holds 8 bf16 values
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& q, float* v) {
+  v[0] = bf16lo(q.x); v[1] = bf16hi(q.x);
+  v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+  v[4] = bf16lo(q.z); v[5] = bf16hi(q.z);
+  v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// |x| as ordered unsigned bits: for non-negative floats (and NaN above inf)
+// integer order equals float order, so max over bits is an exact amax.
+__device__ __forceinline__ uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
+
+// ---------------------------------------------------------------------------
+// E4M3 block scale
+// ---------------------------------------------------------------------------
+// float -> E4M3 code, round-to-nearest-even, saturating to 448 (x >= 0).
+__device__ __forceinline__ uint32_t e4m3_rn_satfinite(float x) {
+  return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// E4M3 code -> float, exact: bias 7, 3 mantissa bits, subnormal step 2^-9.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : __uint_as_float(0x3B000000u /*2^-9*/) * (float)m;
+}
+
+// Per-tensor encode scale s_enc = 2688 / amax (6 * 448), 1 for amax == 0.
+__device__ __forceinline__ float tensor_encode_scale(float amax) {
+  return amax == 0.0f ? 1.0f : __fdiv_rn(2688.0f, amax);
+}
+__device__ __forceinline__ float tensor_decode_scale(float s_enc) { return __fdiv_rn(1.0f, s_enc); }
+
+// Block scale from the block amax: E = e4m3(fl(fl(amax_b / 6) * s_enc)),
+// enc = fl(s_enc / e4m3(E)) or 0 when E == 0.
+__device__ __forceinline__ void block_scale(float amax_b, float s_enc, uint32_t& E, float& enc) {
+  const float sd = __fdiv_rn(amax_b, 6.0f);
+  E = e4m3_rn_satfinite(__fmul_rn(sd, s_enc));
+  enc = E ? __fdiv_rn(s_enc, e4m3_value(E)) : 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+// E2M1 element codes (s.ee.m; magnitudes 0 .5 1 1.5 2 3 4 6)
+// ---------------------------------------------------------------------------
+// Eight values -> four bytes; element 2j in bits 0-3 of byte j.  cvt packs its
+// first source operand into the high nibble.  RNE, saturating at +-6, sign
+// kept for values that round to zero.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Stochastic rounding of one value with a 16-bit uniform u: the lower grid
+// neighbour lo and the spacing give frac = (|v| - lo) / spacing (exact); the
+// value rounds up iff u < frac * 2^16.  |v| >= 6 saturates to 6.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u16) {
+  const uint32_t sign = (__float_as_uint(v) >> 31) << 3;
+  const float a = fabsf(v);
+  if (a >= 6.0f) return sign | 7u;
+  const uint32_t idx = (uint32_t)(a >= 0.5f) + (uint32_t)(a >= 1.0f) + (uint32_t)(a >= 1.5f) +
+                       (uint32_t)(a >= 2.0f) + (uint32_t)(a >= 3.0f) + (uint32_t)(a >= 4.0f);
+  const float lo = idx < 4 ? 0.5f * (float)idx : (float)(idx - 2);
+  const float inv_step = idx < 4 ? 2.0f : (idx < 6 ? 1.0f : 0.5f);
+  const float frac = __fmul_rn(__fsub_rn(a, lo), inv_step);
+  return sign | (idx + (uint32_t)((float)u16 < __fmul_rn(frac, 65536.0f)));
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of
+// (c0,c1,c2,c3) -> (hi(M1 c2)^c1^k0, lo(M1 c2), hi(M0 c0)^c3^k1, lo(M0 c0)),
+// the key bumped by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+struct u32x4 {
+  uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ u32x4 philox4x32_10(u32x4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = u32x4{hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0};
+  }
+  return c;
+}
+
+// The 16 uniforms of 16 consecutive elements starting at e0 (e0 % 8 == 0):
+// two Philox calls with counters (e0/8, e0/8 + 1), low half first.
+__device__ __forceinline__ void sr_uniforms16(uint64_t seed, uint32_t stream, uint64_t e0, uint32_t* u) {
+  const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint64_t g = (e0 >> 3) + h;
+    const u32x4 w = philox4x32_10(u32x4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, k0, k1);
+    u[8 * h + 0] = w.x & 0xFFFFu; u[8 * h + 1] = w.x >> 16;
+    u[8 * h + 2] = w.y & 0xFFFFu; u[8 * h + 3] = w.y >> 16;
+    u[8 * h + 4] = w.z & 0xFFFFu; u[8 * h + 5] = w.z >> 16;
+    u[8 * h + 6] = w.w & 0xFFFFu; u[8 * h + 7] = w.w >> 16;
+  }
+}
+
+// Hadamard sign mask: bit j set -> sign s_j = -1.  Word 0 of
+// Philox(seed, (0, 0, 2, 0)), low 16 bits.
+constexpr uint32_t kRhtStream = 2;
+__device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
+  return philox4x32_10(u32x4{0u, 0u, kRhtStream, 0u}, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
+}
+
+// Q = 1/4 H16 diag(s) on 16 values in registers: sign flips (exact), the
+// in-place butterfly with strides 1, 2, 4, 8 (which sums the products
+// H[i][j] s_j x_j as a pairwise tree in index order), then * 0.25.
+__device__ __forceinline__ void rht16(float* v, uint32_t sign_mask) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((sign_mask >> j) & 1u) << 31));
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+// ---------------------------------------------------------------------------
+// One 1x16 block: amax_b, scale, 16 codes -> (8 code bytes as uint2, E)
+// ---------------------------------------------------------------------------
+template <bool kSR>
+__device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, uint32_t& E, uint64_t seed,
+                                            uint32_t stream, uint64_t e0) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = max(m, abs_bits(v[i]));
+  float enc;
+  block_scale(__uint_as_float(m), s_enc, E, enc);
+  float s[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(v[i], enc);
+  uint2 out;
+  if constexpr (!kSR) {
+    out.x = e2m1x8_rn(s);
+    out.y = e2m1x8_rn(s + 8);
+  } else {
+    uint32_t u[16];
+    sr_uniforms16(seed, stream, e0, u);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lo |= e2m1_sr(s[i], u[i]) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hi |= e2m1_sr(s[8 + i], u[8 + i]) << (4 * i);
+    out.x = lo;
+    out.y = hi;
+  }
+  return out;
+}
+
+// Byte offset of scale (row r, block kb) in the MMA scale layout of a tensor
+// with n_kb = cols/16 blocks per row (n_kb % 4 == 0): 512-byte tiles of 128
+// rows x 4 blocks, row-tile major; (r%32)*16 + ((r/32)%4)*4 + kb%4 inside.
+__device__ __forceinline__ int64_t sf_mma_offset(int64_t r, int64_t kb, int64_t n_kb) {
+  return ((r >> 7) * (n_kb >> 2) + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+__device__ __forceinline__ int64_t sf_offset(int layout, int64_t r, int64_t kb, int64_t n_kb) {
+  return layout ? sf_mma_offset(r, kb, n_kb) : r * n_kb + kb;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,482 @@
+// gemm_kernel.cu -- block-scaled FP4 (NVFP4) GEMM on the sm_103a tensor cores.
+//
+//   D[M, N] = ts_a * ts_b * sum_k e2m1(A[m,k]) e4m3(SA[m,k/16]) e2m1(B[n,k]) e4m3(SB[n,k/16])
+//
+// The GEMMs of "Pretraining Large Language Models with NVFP4" (gist.science
+// summary), Resumo técnico §3 ("Suporte de Hardware": Blackwell tensor cores
+// take NVFP4 natively) -- Fprop, Dgrad and Wgrad of a linear layer, each a
+// product of two K-major NVFP4 operands with FP32 accumulation.
+//
+// Design (one CTA per SM, persistent over 128 x BN output tiles):
+//   warp 0      TMA producer: 2D tiled loads of the packed codes (128-byte
+//               rows, 128B swizzle) and 1D bulk loads of the scale tiles,
+//               into a ring of shared-memory stages guarded by mbarriers.
+//   warp 1      owns the tensor memory; one lane copies each stage's scale
+//               tiles to tensor memory (tcgen05.cp) and issues
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X with
+//               the FP32 accumulator in tensor memory, then tcgen05.commit
+//               frees the stage.
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (each warp reads its
+//               lane quadrant, half of the columns), release the accumulator
+//               to the MMA warp, then scale by ts_a * ts_b, round to BF16 and
+//               store, overlapping the next tile's main loop.
+// Every mbarrier wait is bounded (%globaltimer); on expiry the kernel records
+// NVFP4_ERR_TIMEOUT in the status word, drains its own copies and MMAs,
+// frees tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kBM = 128;          // rows of A per tile (MMA M)
+constexpr int kBKBytes = 128;     // bytes of K per stage per row = 256 FP4 values
+constexpr int kMmaK = 64;         // FP4 values per MMA
+constexpr int kKPerStage = 256;   // FP4 values per stage
+constexpr int kNumThreads = 320;  // 10 warps
+constexpr int kEpiWarps = 8;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kABytes = kBM * kBKBytes;
+  static constexpr int kBBytes = BN * kBKBytes;
+  static constexpr int kSfaBytes = (kBM / 128) * 4 * 512;
+  static constexpr int kSfbBytes = (BN / 128) * 4 * 512;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStages = (220 * 1024) / kStageBytes > 8 ? 8 : (220 * 1024) / kStageBytes;
+  static constexpr int kSfaCol = BN;             // 4 MMAs x 4 columns
+  static constexpr int kSfbCol = BN + 16;        // 4 MMAs x BN/32 columns
+  static constexpr int kTmemCols = (BN + 16 + 4 * (BN / 32)) <= 256 ? 256 : 512;
+  static constexpr int kEpiCols = BN / 2;        // accumulator columns per epilogue warp
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
+};
+
+struct Params {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const float* ts_a;
+  const float* ts_b;
+  void* d;
+  int64_t ldd;
+  int d_f32;
+  int M, N, K;
+  int sf_tiles_k;  // 4-scale tiles per 128-row scale tile row = K / 64
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true when the phase with `parity` completed; false if the
+// kernel is aborting or the wait exceeded kTimeoutNs (which starts the abort).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort = 1;
+        raise_status(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B,
+// 8-row swizzle atoms 1024 B apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Descriptor of a 32-row x 16-byte scale tile (no swizzle): 8-row core
+// matrices of 128 contiguous bytes, 128 B apart.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), K-major,
+// UE4M3 scales, N >> 3 at bit 17, M >> 4 at bit 24, dense K = 64.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int BN>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                      Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar_base = base + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::kStages * C::kStageBytes);
+  // barrier slots: full[S], empty[S], tmem_full, tmem_empty, mma_done
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::kStages + s); };
+  const uint32_t tmem_full = bar_base + 8u * (2 * C::kStages);
+  const uint32_t tmem_empty = tmem_full + 8u;
+  const uint32_t mma_done = tmem_full + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 3);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = p.M / kBM, num_n = p.N / BN;
+  const int n_tiles = num_m * num_n;
+  const int k_stages = (p.K + kKPerStage - 1) / kKPerStage;
+  const int last_nk = ((p.K - 1) % kKPerStage) / kMmaK + 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, kEpiWarps);
+    mbar_init(mma_done, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per-stage bits, for the drain
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int mb = tile % num_m, nb = tile / num_m;
+        for (int ks = 0; ks < k_stages; ++ks) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
+          const int nk = (ks == k_stages - 1) ? last_nk : 4;
+          const uint32_t sf_bytes = (uint32_t)nk * 512u;
+          mbar_arrive_expect_tx(full_bar(stage), C::kABytes + C::kBBytes + sf_bytes * (1 + BN / 128));
+          const uint32_t sa = base + stage * C::kStageBytes;
+          tma_load_2d(sa, &tmap_a, ks * kBKBytes, mb * kBM, full_bar(stage));
+          tma_load_2d(sa + C::kABytes, &tmap_b, ks * kBKBytes, nb * BN, full_bar(stage));
+          const uint32_t sfa_s = sa + C::kABytes + C::kBBytes;
+          bulk_load(sfa_s, p.sfa + ((int64_t)mb * p.sf_tiles_k + ks * 4) * 512, sf_bytes, full_bar(stage));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            bulk_load(sfa_s + C::kSfaBytes + h * 2048,
+                      p.sfb + ((int64_t)(nb * (BN / 128) + h) * p.sf_tiles_k + ks * 4) * 512, sf_bytes,
+                      full_bar(stage));
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // drain: every issued stage's copies have landed before the CTA exits
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued & (1u << s)) {
+          volatile int never = 0;
+          mbar_wait(full_bar(s), (issued_phase >> s) & 1u, &never, p.status);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ----------------------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_mxf4nvf4(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort, p.status)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < k_stages; ++ks) {
+          if (!mbar_wait(full_bar(stage), phase, abort, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const int nk = (ks == k_stages - 1) ? last_nk : 4;
+          const uint32_t sa = base + stage * C::kStageBytes;
+          const uint32_t sb = sa + C::kABytes;
+          const uint32_t sfa_s = sb + C::kBBytes;
+          const uint32_t sfb_s = sfa_s + C::kSfaBytes;
+          for (int j = 0; j < nk; ++j) {
+            tc_cp_sf(tmem + C::kSfaCol + 4 * j, desc_sf(sfa_s + 512 * j));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tc_cp_sf(tmem + C::kSfbCol + (BN / 32) * j + 4 * h, desc_sf(sfb_s + h * 2048 + 512 * j));
+          }
+          for (int j = 0; j < nk; ++j) {
+            tc_mma(tmem, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), idesc, tmem + C::kSfaCol + 4 * j,
+                   tmem + C::kSfbCol + (BN / 32) * j, (ks | j) != 0);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tmem_full);
+        acc_phase ^= 1u;
+      }
+      // all MMAs and copies issued by this thread have finished
+      tc_commit(mma_done);
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, p.status);
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;                 // lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;       // which half of the BN columns
+    const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      const int mb = tile % num_m, nb = tile / num_m;
+      // one lane waits, the warp follows its verdict (tcgen05.ld is warp-wide)
+      int ready = 0;
+      if (lane == 0) ready = mbar_wait(tmem_full, acc_phase, abort, p.status) ? 1 : 0;
+      ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+      if (!ready) break;
+      tc_fence_after();
+      uint32_t v[C::kEpiCols];
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(half * C::kEpiCols);
+#pragma unroll
+      for (int c = 0; c < C::kEpiCols / 32; ++c) tmem_ld32(taddr + 32 * c, v + 32 * c);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+      acc_phase ^= 1u;
+
+      const int64_t row = (int64_t)mb * kBM + 32 * q + lane;
+      const int64_t col0 = (int64_t)nb * BN + half * C::kEpiCols;
+      if (!p.d_f32) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.ldd + col0);
+#pragma unroll
+        for (int c = 0; c < C::kEpiCols / 8; ++c) {
+          uint4 o;
+          o.x = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 0])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 1])));
+          o.y = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 2])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 3])));
+          o.z = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 4])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 5])));
+          o.w = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 6])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 7])));
+          dst[c] = o;
+        }
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0);
+#pragma unroll
+        for (int c = 0; c < C::kEpiCols / 4; ++c) {
+          uint4 o;
+          o.x = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 0])));
+          o.y = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 1])));
+          o.z = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 2])));
+          o.w = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 3])));
+          dst[c] = o;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2D map over packed codes: inner dimension = row bytes, box = 128 B x box_rows.
+bool make_code_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)kBKBytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 152;
+  }
+  return cached[dev];
+}
+
+template <int BN>
+nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
+                 cudaStream_t s) {
+  using C = Cfg<BN>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(nvfp4_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  CUtensorMap ma, mb;
+  const int64_t K = a.cols;
+  if (!make_code_map(&ma, a.codes, (uint64_t)K / 2, (uint64_t)a.rows, kBM) ||
+      !make_code_map(&mb, b.codes, (uint64_t)K / 2, (uint64_t)b.rows, BN))
+    return NVFP4_ERR_CUDA;
+  Params p;
+  p.sfa = a.scales;
+  p.sfb = b.scales;
+  p.ts_a = a.tensor_scale;
+  p.ts_b = b.tensor_scale;
+  p.d = d;
+  p.ldd = ldd;
+  p.d_f32 = d_dtype == NVFP4_OUT_F32;
+  p.M = (int)a.rows;
+  p.N = (int)b.rows;
+  p.K = (int)K;
+  p.sf_tiles_k = (int)(K / 64);
+  p.status = device_status_ptr();
+  const int tiles = (p.M / kBM) * (p.N / BN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  nvfp4_gemm_kernel<BN><<<grid, kNumThreads, C::kSmemBytes, s>>>(ma, mb, p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace
+
+nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
+                         cudaStream_t s) {
+  if (b.rows % 256 == 0) return run<256>(a, b, d, d_dtype, ldd, s);
+  return run<128>(a, b, d, d_dtype, ldd, s);
+}
+
+}  // namespace nvfp4

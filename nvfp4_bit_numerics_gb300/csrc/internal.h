@@ -1,0 +1,48 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "nvfp4.h"
+
+namespace nvfp4 {
+
+// Bits of the per-device status word.
+constexpr uint32_t kStatusNonFinite = 1u << 4;
+constexpr uint32_t kStatusTimeout = 1u << 5;
+
+// Per-device status word (a __device__ variable of api.cu), as a device
+// address usable by kernels of every translation unit.  Sets cudaError on
+// failure and returns nullptr.
+uint32_t* device_status_ptr();
+
+// Host-side count of kernels launched by the library (for the bench's
+// launch accounting).
+extern std::atomic<uint64_t> g_launches;
+inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Quantize launchers (quant_kernels.cu).  Arguments are already validated.
+// Each non-null output is zeroed and then receives its amax: max|x|, max|Qx|
+// with Q along the contiguous dimension, max|Qx| with Q along rows.
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, float* plain, float* rht_rows, float* rht_cols,
+                        uint64_t rht_seed, cudaStream_t s);
+cudaError_t launch_quant_rowwise(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor& out,
+                                 const float* amax, bool rht, bool sr, uint64_t seed, uint32_t stream_id,
+                                 cudaStream_t s);
+cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor* out_row,
+                              const float* amax_row, const nvfp4_tensor* out_t, const float* amax_t,
+                              bool rht_t, bool sr, uint64_t seed, uint32_t stream_row, uint32_t stream_t,
+                              cudaStream_t s);
+cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvfp4_tensor& out,
+                            const nvfp4_tensor* out_t, const float* amax, cudaStream_t s);
+
+// GEMM launcher (gemm_kernel.cu).  Arguments are already validated.
+nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
+                         cudaStream_t s);
+
+}  // namespace nvfp4

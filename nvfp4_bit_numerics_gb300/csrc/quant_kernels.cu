@@ -1,0 +1,424 @@
+// quant_kernels.cu -- bandwidth-bound NVFP4 kernels for sm_103a: global
+// amax, 1x16 rowwise quantization, the 64x64 tile kernel that writes the
+// rowwise and/or the transposed (token-major, Hadamard-transformed) operand
+// from one read, and the 16x16 2D weight quantization that writes W and W^T.
+//
+// Method: "Pretraining Large Language Models with NVFP4" (gist.science
+// summary), Resumo técnico §2 Metodologia: two-level NVFP4 scaling ("Escala
+// em Dois Níveis"), random Hadamard transform on the Wgrad inputs (item 2),
+// 2D 16x16 weight scaling (item 3), stochastic rounding of gradients (item 4).
+//
+// All kernels read BF16 with 16-byte vector loads, keep their working set in
+// registers or a small shared-memory tile, and write packed codes with 8- or
+// 16-byte stores; they are bound by HBM bandwidth.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kThreads = 256;
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 152;
+  }
+  return cached[dev];
+}
+
+int grid_for(int64_t units, int per_sm) {
+  const int64_t cap = (int64_t)sm_count() * per_sm;
+  const int64_t need = (units + kThreads - 1) / kThreads;
+  return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+__device__ __forceinline__ void warp_amax_to_global(uint32_t m, uint32_t* out, uint32_t* status) {
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31) == 0 && m) {
+    atomicMax(out, m);
+    if (m >= 0x7F800000u) raise_status(status, kStatusNonFinite);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// amax kernels.  out[] holds float bits; the caller zeroes it first.
+// ---------------------------------------------------------------------------
+
+// max |x| over n_vec 16-byte vectors, in the bf16 bit domain (two halves per
+// word compared with a SIMD max), converted to float bits at the end.
+__global__ void __launch_bounds__(kThreads) amax_plain_kernel(const uint4* __restrict__ x, int64_t n_vec,
+                                                              uint32_t* out, uint32_t* status) {
+  uint32_t m2 = 0;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  for (; i + 3 * stride < n_vec; i += 4 * stride) {
+    uint4 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) q[u] = ldg_nc_v4(x + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      m2 = __vmaxu2(__vmaxu2(m2, q[u].x & 0x7FFF7FFFu),
+                    __vmaxu2(__vmaxu2(q[u].y & 0x7FFF7FFFu, q[u].z & 0x7FFF7FFFu), q[u].w & 0x7FFF7FFFu));
+  }
+  for (; i < n_vec; i += stride) {
+    const uint4 q = ldg_nc_v4(x + i);
+    m2 = __vmaxu2(__vmaxu2(m2, q.x & 0x7FFF7FFFu),
+                  __vmaxu2(__vmaxu2(q.y & 0x7FFF7FFFu, q.z & 0x7FFF7FFFu), q.w & 0x7FFF7FFFu));
+  }
+  const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+  warp_amax_to_global(m, out, status);
+}
+
+// Plain amax and amax of the 16-point transform along the contiguous
+// dimension: one thread per 16-element chunk of a row.
+__global__ void __launch_bounds__(kThreads) amax_rht_rows_kernel(const uint4* __restrict__ x, int64_t n_chunks,
+                                                                 uint64_t seed, uint32_t* out_plain,
+                                                                 uint32_t* out_rht, uint32_t* status) {
+  const uint32_t smask = rht_sign_mask(seed);
+  uint32_t mp = 0, mr = 0;
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n_chunks; i += (int64_t)gridDim.x * kThreads) {
+    float v[16];
+    unpack8(ldg_nc_v4(x + 2 * i), v);
+    unpack8(ldg_nc_v4(x + 2 * i + 1), v + 8);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mp = max(mp, abs_bits(v[j]));
+    rht16(v, smask);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mr = max(mr, abs_bits(v[j]));
+  }
+  if (out_plain) warp_amax_to_global(mp, out_plain, status);
+  warp_amax_to_global(mr, out_rht, status);
+}
+
+// Plain amax and amax of the 16-point transform along the rows (tokens):
+// one thread per (16-row block, 8-column group); a warp reads 512
+// contiguous bytes of each of the 16 rows.
+__global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                 int64_t cols, uint64_t seed, uint32_t* out_plain,
+                                                                 uint32_t* out_rht, uint32_t* status) {
+  const uint32_t smask = rht_sign_mask(seed);
+  const int64_t groups = cols >> 3;
+  const int64_t units = (rows >> 4) * groups;
+  uint32_t mp = 0, mr = 0;
+  for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += (int64_t)gridDim.x * kThreads) {
+    const int64_t rb = u / groups, cg = u - rb * groups;
+    const uint16_t* p = x + (rb * 16) * cols + cg * 8;
+    uint4 q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = ldg_nc_v4(p + i * cols);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t w = (c < 2) ? q[i].x : (c < 4) ? q[i].y : (c < 6) ? q[i].z : q[i].w;
+        v[i] = (c & 1) ? bf16hi(w) : bf16lo(w);
+        mp = max(mp, abs_bits(v[i]));
+      }
+      rht16(v, smask);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mr = max(mr, abs_bits(v[i]));
+    }
+  }
+  if (out_plain) warp_amax_to_global(mp, out_plain, status);
+  warp_amax_to_global(mr, out_rht, status);
+}
+
+// ---------------------------------------------------------------------------
+// Shared per-tensor prologue: s_enc from the amax; block 0 stores ts and
+// flags a non-finite amax.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float tensor_prologue(const float* amax, float* ts_out, uint32_t* status) {
+  const float a = *amax;
+  const float s_enc = tensor_encode_scale(a);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (ts_out) *ts_out = tensor_decode_scale(s_enc);
+    if (!(abs_bits(a) < 0x7F800000u)) raise_status(status, kStatusNonFinite);
+  }
+  return s_enc;
+}
+
+// ---------------------------------------------------------------------------
+// 1x16 rowwise quantization: one thread per 64 elements (4 blocks) of a row.
+// ---------------------------------------------------------------------------
+template <bool kSR, bool kRHT>
+__global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                 int64_t cols, const float* amax, uint8_t* codes,
+                                                                 uint8_t* scales, int layout, float* ts_out,
+                                                                 uint64_t seed, uint32_t stream, uint32_t* status) {
+  const float s_enc = tensor_prologue(amax, ts_out, status);
+  const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
+  const int64_t gpr = cols >> 6;  // 64-element groups per row
+  const int64_t units = rows * gpr;
+  const int64_t n_kb = cols >> 4;
+  for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += (int64_t)gridDim.x * kThreads) {
+    const int64_t r = u / gpr, g = u - r * gpr;
+    const int64_t c0 = g * 64;
+    const uint16_t* p = x + r * cols + c0;
+    uint4 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = ldg_nc_v4(p + 8 * i);
+    uint32_t cw[8];
+    uint32_t sc = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float v[16];
+      unpack8(q[2 * b], v);
+      unpack8(q[2 * b + 1], v + 8);
+      if constexpr (kRHT) rht16(v, smask);
+      uint32_t E;
+      const uint2 o = quantize16<kSR>(v, s_enc, E, seed, stream, (uint64_t)(r * cols + c0 + 16 * b));
+      cw[2 * b] = o.x;
+      cw[2 * b + 1] = o.y;
+      sc |= E << (8 * b);
+    }
+    uint4* cp = reinterpret_cast<uint4*>(codes + r * (cols >> 1) + (c0 >> 1));
+    cp[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    cp[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    *reinterpret_cast<uint32_t*>(scales + sf_offset(layout, r, c0 >> 4, n_kb)) = sc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 64x64 tile kernel: one read of x [rows, cols] BF16 into shared memory, then
+//  - rowwise:    1x16 blocks along cols of x       -> out_row [rows, cols]
+//  - transposed: 1x16 blocks along rows of x (after the optional 16-point
+//                transform along rows)             -> out_t   [cols, rows]
+// ---------------------------------------------------------------------------
+struct TileOut {
+  uint8_t* codes;
+  uint8_t* scales;
+  const float* amax;
+  float* ts;
+  int layout;
+  uint32_t stream;
+};
+
+constexpr int kTile = 64;
+constexpr int kTilePitch = 72;  // uint16 per smem row: 144 B, conflict-free 16 B row reads
+
+template <bool kRow, bool kT, bool kRHT, bool kSR>
+__global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                              int64_t cols, TileOut orow, TileOut ot,
+                                                              uint64_t seed, uint32_t* status) {
+  __shared__ __align__(16) uint16_t tile[kTile * kTilePitch];
+  const int t = threadIdx.x;
+  const int64_t tiles_c = cols / kTile;
+  const int64_t tm = blockIdx.x / tiles_c, tc = blockIdx.x - tm * tiles_c;
+  const int64_t m0 = tm * kTile, c0 = tc * kTile;
+
+  float s_row = 1.0f, s_t = 1.0f;
+  if constexpr (kRow) s_row = tensor_prologue(orow.amax, orow.ts, status);
+  if constexpr (kT) s_t = tensor_prologue(ot.amax, ot.ts, status);
+
+  // load: 64 rows x 8 vectors of 16 B
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int v = t + k * kThreads;
+    const int row = v >> 3, cv = v & 7;
+    const uint4 q = ldg_nc_v4(x + (m0 + row) * cols + c0 + cv * 8);
+    *reinterpret_cast<uint4*>(&tile[row * kTilePitch + cv * 8]) = q;
+  }
+  __syncthreads();
+
+  if constexpr (kRow) {
+    const int r = t >> 2, bc = t & 3;
+    const uint4* sp = reinterpret_cast<const uint4*>(&tile[r * kTilePitch + bc * 16]);
+    float v[16];
+    unpack8(sp[0], v);
+    unpack8(sp[1], v + 8);
+    uint32_t E;
+    const int64_t gr = m0 + r, gc = c0 + bc * 16;
+    const uint2 o = quantize16<kSR>(v, s_row, E, seed, orow.stream, (uint64_t)(gr * cols + gc));
+    *reinterpret_cast<uint2*>(orow.codes + gr * (cols >> 1) + (gc >> 1)) = o;
+    orow.scales[sf_offset(orow.layout, gr, gc >> 4, cols >> 4)] = (uint8_t)E;
+  }
+  if constexpr (kT) {
+    const int c = t & 63, mc = t >> 6;
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[(16 * mc + i) * kTilePitch + c] << 16);
+    if constexpr (kRHT) rht16(v, rht_sign_mask(seed));
+    uint32_t E;
+    const int64_t gr = c0 + c, gm = m0 + 16 * mc;  // row / column of the transposed tensor
+    const uint2 o = quantize16<kSR>(v, s_t, E, seed, ot.stream, (uint64_t)(gr * rows + gm));
+    *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = o;
+    ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)E;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2D weight quantization, 64x64 tile = 4x4 blocks of 16x16.  Thread t holds
+// row t/4, block column t%4 (16 elements).  Writes W's codes directly and
+// W^T's codes through a shared-memory transpose of the 4-bit codes.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) quant_2d_kernel(const uint16_t* __restrict__ w, int64_t rows,
+                                                            int64_t cols, const float* amax, TileOut ow,
+                                                            TileOut owt, int has_t, uint32_t* status) {
+  __shared__ uint32_t s_amax[8][4];
+  __shared__ uint32_t s_E[4][4];
+  __shared__ uint8_t s_codes[kTile][kTile];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int64_t tiles_c = cols / kTile;
+  const int64_t tm = blockIdx.x / tiles_c, tc = blockIdx.x - tm * tiles_c;
+  const int64_t r0 = tm * kTile, c0 = tc * kTile;
+  const float s_enc = tensor_prologue(amax, ow.ts, status);
+  if (has_t && blockIdx.x == 0 && t == 0) *owt.ts = tensor_decode_scale(s_enc);
+
+  const int r = t >> 2, bc = t & 3;
+  const uint16_t* p = w + (r0 + r) * cols + c0 + bc * 16;
+  float v[16];
+  unpack8(ldg_nc_v4(p), v);
+  unpack8(ldg_nc_v4(p + 8), v + 8);
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = max(m, abs_bits(v[i]));
+  // lanes 4r'+bc of this warp hold rows 8*warp + r' of block column bc
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+  if (lane < 4) s_amax[warp][lane] = m;
+  __syncthreads();
+  const int br = r >> 4;
+  const uint32_t mb = max(s_amax[2 * br][bc], s_amax[2 * br + 1][bc]);
+  uint32_t E;
+  float enc;
+  block_scale(__uint_as_float(mb), s_enc, E, enc);
+  float s[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(v[i], enc);
+  const uint32_t lo = e2m1x8_rn(s), hi = e2m1x8_rn(s + 8);
+  const int64_t gr = r0 + r, gc = c0 + bc * 16;
+  *reinterpret_cast<uint2*>(ow.codes + gr * (cols >> 1) + (gc >> 1)) = make_uint2(lo, hi);
+  ow.scales[sf_offset(ow.layout, gr, gc >> 4, cols >> 4)] = (uint8_t)E;
+  if (!has_t) return;
+
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    s_codes[r][bc * 16 + i] = (lo >> (4 * i)) & 15u;
+    s_codes[r][bc * 16 + 8 + i] = (hi >> (4 * i)) & 15u;
+  }
+  if ((r & 15) == 0) s_E[br][bc] = E;
+  __syncthreads();
+  // thread t -> row k = t/4 of the W^T tile (column k of W), chunk nc = t%4
+  const int k = t >> 2, nc = t & 3;
+  uint32_t tw[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) tw[i >> 3] |= (uint32_t)s_codes[16 * nc + i][k] << (4 * (i & 7));
+  const int64_t tr = c0 + k, tcol = r0 + 16 * nc;
+  *reinterpret_cast<uint2*>(owt.codes + tr * (rows >> 1) + (tcol >> 1)) = make_uint2(tw[0], tw[1]);
+  owt.scales[sf_offset(owt.layout, tr, tcol >> 4, rows >> 4)] = (uint8_t)s_E[nc][k >> 4];
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, float* plain, float* rht_rows, float* rht_cols,
+                        uint64_t rht_seed, cudaStream_t s) {
+  uint32_t* status = device_status_ptr();
+  uint32_t* o_plain = reinterpret_cast<uint32_t*>(plain);
+  uint32_t* o_rows = reinterpret_cast<uint32_t*>(rht_rows);
+  uint32_t* o_cols = reinterpret_cast<uint32_t*>(rht_cols);
+  for (uint32_t* o : {o_plain, o_rows, o_cols}) {
+    if (!o) continue;
+    const cudaError_t e = cudaMemsetAsync(o, 0, 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t n = rows * cols;
+  if (n == 0) return cudaSuccess;
+  // the plain amax rides along with the first transform pass that runs
+  if (o_cols) {
+    const int64_t units = (rows / 16) * (cols / 8);
+    amax_rht_cols_kernel<<<grid_for(units, 4), kThreads, 0, s>>>(static_cast<const uint16_t*>(x), rows, cols,
+                                                                 rht_seed, o_plain, o_cols, status);
+    count_launch();
+    o_plain = nullptr;
+  }
+  if (o_rows) {
+    const int64_t units = n / 16;
+    amax_rht_rows_kernel<<<grid_for(units, 8), kThreads, 0, s>>>(static_cast<const uint4*>(x), units, rht_seed,
+                                                                 o_plain, o_rows, status);
+    count_launch();
+    o_plain = nullptr;
+  }
+  if (o_plain) {
+    const int64_t nv = n / 8;
+    amax_plain_kernel<<<grid_for(nv / 4 + 1, 8), kThreads, 0, s>>>(static_cast<const uint4*>(x), nv, o_plain,
+                                                                   status);
+    count_launch();
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rowwise(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor& out,
+                                 const float* amax, bool rht, bool sr, uint64_t seed, uint32_t stream_id,
+                                 cudaStream_t s) {
+  const int64_t units = rows * (cols / 64);
+  const int grid = grid_for(units, 8);
+  auto args = [&](auto kern) {
+    kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), rows, cols, amax, out.codes, out.scales,
+                                   out.scale_layout, out.tensor_scale, seed, stream_id, device_status_ptr());
+  };
+  if (sr) {
+    if (rht) args(quant_rowwise_kernel<true, true>);
+    else args(quant_rowwise_kernel<true, false>);
+  } else {
+    if (rht) args(quant_rowwise_kernel<false, true>);
+    else args(quant_rowwise_kernel<false, false>);
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor* out_row,
+                              const float* amax_row, const nvfp4_tensor* out_t, const float* amax_t, bool rht_t,
+                              bool sr, uint64_t seed, uint32_t stream_row, uint32_t stream_t, cudaStream_t s) {
+  TileOut orow{}, ot{};
+  if (out_row) orow = TileOut{out_row->codes, out_row->scales, amax_row, out_row->tensor_scale, out_row->scale_layout,
+                              stream_row};
+  if (out_t) ot = TileOut{out_t->codes, out_t->scales, amax_t, out_t->tensor_scale, out_t->scale_layout, stream_t};
+  const int64_t tiles = (rows / kTile) * (cols / kTile);
+  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)tiles);
+  uint32_t* status = device_status_ptr();
+  const uint16_t* xp = static_cast<const uint16_t*>(x);
+  const bool row = out_row != nullptr, tr = out_t != nullptr;
+#define NVFP4_TILE(R, T, H, S) quant_tile_kernel<R, T, H, S><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot, seed, status)
+  if (row && tr) {
+    if (rht_t) { if (sr) NVFP4_TILE(true, true, true, true); else NVFP4_TILE(true, true, true, false); }
+    else       { if (sr) NVFP4_TILE(true, true, false, true); else NVFP4_TILE(true, true, false, false); }
+  } else if (tr) {
+    if (rht_t) { if (sr) NVFP4_TILE(false, true, true, true); else NVFP4_TILE(false, true, true, false); }
+    else       { if (sr) NVFP4_TILE(false, true, false, true); else NVFP4_TILE(false, true, false, false); }
+  } else {
+    if (sr) NVFP4_TILE(true, false, false, true); else NVFP4_TILE(true, false, false, false);
+  }
+#undef NVFP4_TILE
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvfp4_tensor& out,
+                            const nvfp4_tensor* out_t, const float* amax, cudaStream_t s) {
+  TileOut ow{out.codes, out.scales, amax, out.tensor_scale, out.scale_layout, 0};
+  TileOut owt{};
+  if (out_t) owt = TileOut{out_t->codes, out_t->scales, amax, out_t->tensor_scale, out_t->scale_layout, 0};
+  const int64_t tiles = (rows / kTile) * (cols / kTile);
+  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  quant_2d_kernel<<<(unsigned)tiles, kThreads, 0, s>>>(static_cast<const uint16_t*>(w), rows, cols, amax, ow, owt,
+                                                       out_t ? 1 : 0, device_status_ptr());
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -176,15 +176,17 @@ def quantize_2d(w, amax=None):
     )
 
 
-def amax_rht(x, rht_seed, axis, chunk_rows=4096):
-    """amax of the tensor after the 16-chunk Hadamard transform along ``axis``."""
+def amax_rht(x, rht_seed, axis, chunk_elems=1 << 21):
+    """amax of the tensor after the 16-chunk Hadamard transform along ``axis``
+    (processed in slices of whole 16-chunks to bound memory)."""
     x = np.asarray(x, dtype=np.float32)
     signs = rht_signs(rht_seed)
     other = 1 - axis
-    best = F32(0.0)
     n = x.shape[other]
-    for s in range(0, n, chunk_rows):
-        part = x[s:s + chunk_rows] if other == 0 else x[:, s:s + chunk_rows]
+    step = max(1, chunk_elems // max(1, x.shape[axis]))
+    best = F32(0.0)
+    for s in range(0, n, step):
+        part = x[s:s + step] if other == 0 else x[:, s:s + step]
         if part.size:
             best = max(best, F32(np.max(np.abs(rht_along_axis(part, signs, axis)))))
     return F32(best)

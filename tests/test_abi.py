@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/nvfp4.h declares; host-side argument checks reject bad calls before
+any launch (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from nvfp4_bit_numerics_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "nvfp4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(binding.EXPORTED) == sorted(n for n in names)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.nvfp4_status_string(code)
+    assert lib.nvfp4_status_string(99) == b"unknown status"
+
+
+def test_size_queries(lib):
+    assert binding.nvfp4_scale_bytes(128, 256, binding.NVFP4_SCALES_MMA) == 128 * 16
+    assert binding.nvfp4_scale_bytes(256, 64, binding.NVFP4_SCALES_MMA) == 1024
+    assert binding.nvfp4_scale_bytes(100, 64, binding.NVFP4_SCALES_LINEAR) == 400
+    ws = binding.nvfp4_linear_workspace_bytes(128, 256, 256)
+    # six tensors, 0.5 B codes + 1/16 B scales per element, plus a header
+    elems = 2 * 128 * 256 + 2 * 256 * 256 + 2 * 256 * 128
+    assert ws >= elems * 0.5625 + 256
+    assert binding.nvfp4_linear_workspace_bytes(0, 1, 1) == 0
+
+
+def _t(rows, cols, layout=1, codes=16, scales=16, amax=16, ts=16):
+    return binding.nvfp4_tensor(codes, scales, amax, ts, rows, cols, layout, 0)
+
+
+def test_gemm_argument_checks(lib):
+    a, b = _t(128, 256), _t(256, 256)
+    d = ctypes.c_void_p(16)
+    call = lambda a_, b_, d_=d, dt=0, ldd=256: lib.nvfp4_gemm(ctypes.byref(a_), ctypes.byref(b_), d_, dt, ldd, None)
+    assert lib.nvfp4_gemm(None, ctypes.byref(b), d, 0, 256, None) == binding.NVFP4_ERR_ARG
+    assert call(a, b, d_=None) == binding.NVFP4_ERR_ARG
+    assert call(a, b, dt=7) == binding.NVFP4_ERR_ARG
+    assert call(_t(128, 256, layout=0), b) == binding.NVFP4_ERR_ARG
+    assert call(_t(100, 256), b) == binding.NVFP4_ERR_SHAPE
+    assert call(a, _t(256, 128)) == binding.NVFP4_ERR_SHAPE
+    assert call(_t(128, 96), _t(256, 96)) == binding.NVFP4_ERR_SHAPE
+    assert call(a, b, ldd=200) == binding.NVFP4_ERR_SHAPE
+    assert call(a, _t(256, 256, codes=24)) == binding.NVFP4_ERR_ARG
+    assert call(a, b, d_=ctypes.c_void_p(24)) == binding.NVFP4_ERR_ALIGN
+    assert call(a, b, ldd=260) == binding.NVFP4_ERR_ALIGN
+
+
+def test_quantize_argument_checks(lib):
+    cfg = binding.nvfp4_quant_cfg(0, 0, 0, 0, 0, 0, 0)
+    out = _t(128, 256)
+    x = ctypes.c_void_p(16)
+    q = lambda x_=x, r=128, c=256, cfg_=cfg, o=out: lib.nvfp4_quantize(x_, r, c, ctypes.byref(cfg_),
+                                                                    ctypes.byref(o), None, None)
+    assert q(x_=None) == binding.NVFP4_ERR_ARG
+    assert q(r=100) == binding.NVFP4_ERR_SHAPE
+    assert q(c=0) == binding.NVFP4_ERR_SHAPE
+    assert q(x_=ctypes.c_void_p(8)) == binding.NVFP4_ERR_ALIGN
+    assert q(o=_t(128, 128)) == binding.NVFP4_ERR_SHAPE
+    assert q(o=_t(64, 256)) == binding.NVFP4_ERR_SHAPE
+    assert q(cfg_=binding.nvfp4_quant_cfg(9, 0, 0, 0, 0, 0, 0)) == binding.NVFP4_ERR_ARG
+    assert q(cfg_=binding.nvfp4_quant_cfg(0, 5, 0, 0, 0, 0, 0)) == binding.NVFP4_ERR_ARG
+    # fused kind needs the transposed output
+    assert q(cfg_=binding.nvfp4_quant_cfg(2, 0, 0, 0, 0, 0, 0)) == binding.NVFP4_ERR_ARG
+    assert lib.nvfp4_amax(x, 10, 17, 1, 0, ctypes.c_void_p(16), None) == binding.NVFP4_ERR_SHAPE
+    assert lib.nvfp4_amax(x, 10, 16, 4, 0, ctypes.c_void_p(16), None) == binding.NVFP4_ERR_SHAPE
+    assert lib.nvfp4_amax(x, 16, 16, 0, 0, ctypes.c_void_p(16), None) == binding.NVFP4_ERR_ARG
+
+
+def test_linear_argument_checks(lib):
+    ws = binding.nvfp4_linear_workspace_bytes(128, 256, 256)
+    p = ctypes.c_void_p(16)
+    f = lambda M=128, K=256, N=256, wsb=ws, w=p: lib.nvfp4_linear_fwd(p, p, M, K, N, 1, p, w, wsb, None)
+    assert f(M=64) == binding.NVFP4_ERR_SHAPE
+    assert f(wsb=ws - 1) == binding.NVFP4_ERR_WORKSPACE
+    assert f(w=None) == binding.NVFP4_ERR_ARG
+    assert f(w=ctypes.c_void_p(8)) == binding.NVFP4_ERR_ALIGN
+    assert lib.nvfp4_linear_bwd(p, 128, 256, 256, 1, p, None, p, ws, None) == binding.NVFP4_ERR_ARG

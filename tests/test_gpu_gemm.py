@@ -1,0 +1,125 @@
+"""GPU parity of the block-scaled FP4 GEMM against the oracle's FP64 GEMM on
+the dequantized operands.  One-hot probes pin the operand nibble order, the
+row mapping and the scale-factor layout that the tensor cores consume."""
+
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_bit_numerics_gb300 import binding as B
+from oracle import formats, gemm, quant
+from tests.gpu_util import ensure_lib, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    return ensure_lib()
+
+
+def make_q(codes_u4, scales_lin, ts):
+    """Device QTensor from unpacked 4-bit codes [rows, K] and linear E4M3
+    scale codes [rows, K/16] (the scales are put in the MMA layout by the
+    oracle's layout definition)."""
+    rows, K = codes_u4.shape
+    q = B.QTensor(
+        torch.from_numpy(formats.pack_nibbles(codes_u4)).cuda(),
+        torch.from_numpy(quant.swizzle_scales(scales_lin)).cuda(),
+        torch.zeros(1, dtype=torch.float32, device="cuda"),
+        torch.tensor([ts], dtype=torch.float32, device="cuda"),
+        rows, K, B.NVFP4_SCALES_MMA)
+    return q
+
+
+def ref_gemm(ac, asc, ta, bc, bsc, tb):
+    return gemm.gemm_ref(formats.pack_nibbles(ac), asc, np.float32(ta), formats.pack_nibbles(bc), bsc,
+                         np.float32(tb))
+
+
+@pytest.mark.parametrize("N", [128, 256])
+def test_one_hot_layout_probe(N):
+    """A single nonzero in A (row i, element k) and in B (row j, element k)
+    must land at D[i, j] only, scaled by exactly the block scales of
+    (i, k/16) and (j, k/16); every other block carries a different scale."""
+    M, K = 128, 512
+    rng = np.random.default_rng(0)
+    positions = [(0, 0, 0), (1, 1, 1), (37, 63, 200), (127, 64, N - 1), (64, 255, 128 % N), (33, 256, 7),
+                 (96, 511, N // 2 + 3), (31, 300, 32), (32, 301, 31)]
+    for (i, k, j) in positions:
+        j = j % N
+        ac = np.zeros((M, K), np.uint8)
+        bc = np.zeros((N, K), np.uint8)
+        ac[i, k] = 7        # +6
+        bc[j, k] = 0xB      # -1.5
+        asc = rng.integers(0x30, 0x40, size=(M, K // 16)).astype(np.uint8)
+        bsc = rng.integers(0x40, 0x50, size=(N, K // 16)).astype(np.uint8)
+        asc[i, k // 16] = 0x41  # 2.25
+        bsc[j, k // 16] = 0x3C  # 1.5
+        d = B.nvfp4_gemm(make_q(ac, asc, 1.0), make_q(bc, bsc, 1.0), out_dtype=torch.float32).cpu().numpy()
+        nz = np.argwhere(d != 0)
+        assert nz.tolist() == [[i, j]], ((i, k, j), nz[:5].tolist())
+        assert d[i, j] == 6.0 * 2.25 * -1.5 * 1.5, ((i, k, j), d[i, j])
+
+
+def test_tiny_exact_fp32():
+    """K = 64 with unit scales: every FP32 partial sum is exact, so the FP32
+    output equals the oracle bit for bit."""
+    rng = np.random.default_rng(1)
+    M, N, K = 128, 256, 64
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    one = lambda r: np.full((r, K // 16), 0x38, np.uint8)
+    d = B.nvfp4_gemm(make_q(ac, one(M), 1.0), make_q(bc, one(N), 1.0), out_dtype=torch.float32).cpu().numpy()
+    ref = ref_gemm(ac, one(M), 1.0, bc, one(N), 1.0)
+    np.testing.assert_array_equal(d.astype(np.float64), ref)
+
+
+GEMM_SHAPES = [(128, 256, 256), (256, 512, 1024), (384, 384, 320), (128, 128, 192), (512, 768, 2048),
+               (256, 256, 64), (1024, 1280, 1536)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_random_gemm(M, N, K):
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    asc = rng.integers(0x20, 0x60, size=(M, K // 16)).astype(np.uint8)
+    bsc = rng.integers(0x20, 0x60, size=(N, K // 16)).astype(np.uint8)
+    ta, tb = 0.013, 0.37
+    qa, qb = make_q(ac, asc, ta), make_q(bc, bsc, tb)
+    ref = ref_gemm(ac, asc, ta, bc, bsc, tb)
+    d32 = B.nvfp4_gemm(qa, qb, out_dtype=torch.float32).cpu().numpy()
+    assert rel_fro(d32, ref) <= 1e-5
+    d16 = B.nvfp4_gemm(qa, qb).float().cpu().numpy()
+    assert rel_fro(d16, formats.float64_to_bf16_rne(ref)) <= 1e-3
+    assert rel_fro(d16, ref) <= 4e-3  # BF16 output rounding alone
+
+
+def test_strided_output():
+    rng = np.random.default_rng(3)
+    M, N, K = 128, 256, 256
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    sc = lambda r: rng.integers(0x30, 0x40, size=(r, K // 16)).astype(np.uint8)
+    asc, bsc = sc(M), sc(N)
+    out = torch.full((M, N + 64), 7.0, dtype=torch.float32, device="cuda")
+    B.nvfp4_gemm(make_q(ac, asc, 1.0), make_q(bc, bsc, 1.0), out=out[:, :N])
+    o = out.cpu().numpy()
+    assert np.all(o[:, N:] == 7.0)
+    assert rel_fro(o[:, :N], ref_gemm(ac, asc, 1.0, bc, bsc, 1.0)) <= 1e-5
+
+
+def test_gemm_repeatable():
+    rng = np.random.default_rng(4)
+    M, N, K = 256, 512, 768
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    asc = rng.integers(0x30, 0x40, size=(M, K // 16)).astype(np.uint8)
+    bsc = rng.integers(0x30, 0x40, size=(N, K // 16)).astype(np.uint8)
+    qa, qb = make_q(ac, asc, 1.0), make_q(bc, bsc, 1.0)
+    a = B.nvfp4_gemm(qa, qb)
+    b = B.nvfp4_gemm(qa, qb)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert B.nvfp4_get_status() == B.NVFP4_OK
