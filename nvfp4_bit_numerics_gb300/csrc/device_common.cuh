@@ -154,7 +154,10 @@ __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
 
 // Q = 1/4 H16 diag(s) on 16 values in registers: sign flips (exact), the
 // in-place butterfly with strides 1, 2, 4, 8 (which sums the products
-// H[i][j] s_j x_j as a pairwise tree in index order), then * 0.25.
+// H[i][j] s_j x_j as a pairwise tree in index order), then * 0.25.  A zero
+// has no sign in Q x, so exact-zero outputs are made +0 (adding +0 does
+// that and leaves every other value unchanged); the butterfly and other
+// summation orders differ only in the sign of exact zeros.
 __device__ __forceinline__ void rht16(float* v, uint32_t sign_mask) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((sign_mask >> j) & 1u) << 31));
@@ -170,7 +173,7 @@ __device__ __forceinline__ void rht16(float* v, uint32_t sign_mask) {
     }
   }
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+  for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(__fmul_rn(v[j], 0.25f), 0.0f);
 }
 
 // ---------------------------------------------------------------------------

@@ -16,7 +16,10 @@ Readings (the pages give no formula):
   transformed axis, so Q^T Q = I;
 * float32 arithmetic: the products H[i][j]·s[j]·x[j] are exact sign flips,
   they are summed as a pairwise tree in index order (pairs (0,1), (2,3), ...,
-  then pairs of pairs), and the sum is multiplied by 0.25.
+  then pairs of pairs), and the sum is multiplied by 0.25;
+* a zero has no sign in Q x: an output that is exactly zero is +0 (any
+  summation order gives the same nonzero results bit for bit, but the sign of
+  an exact zero depends on where negations are applied).
 """
 
 import numpy as np
@@ -60,7 +63,8 @@ def rht16_chunks(x, signs):
     # terms[..., i, j] = H[i][j]·s[j]·x[j], exact
     terms = coef * x[..., None, :]
     y = _tree_sum_f32(terms)
-    return (y * np.float32(0.25)).astype(np.float32)
+    y = (y * np.float32(0.25)).astype(np.float32)
+    return (y + np.float32(0.0)).astype(np.float32)  # -0 -> +0
 
 
 def rht_along_axis(x, signs, axis):

@@ -119,12 +119,17 @@ def test_edge_values_and_ties():
 
 
 def test_zero_tensor():
+    """amax = 0: s_enc = ts = 1 and every scale is 0.  The rowwise codes are
+    +0; the Hadamard sign flips give signed zeros in the transposed output,
+    whose codes (0x0 or 0x8) must match the oracle's."""
     x = torch.zeros(128, 256, dtype=torch.bfloat16)
     out, out_t = B.nvfp4_quantize(x.cuda(), B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, rht=True, seed=1)
     torch.cuda.synchronize()
     for q in (out, out_t):
         assert q.tensor_scale.item() == 1.0 and q.amax.item() == 0.0
-        assert int(q.codes.count_nonzero()) == 0 and int(q.scales.count_nonzero()) == 0
+        assert int(q.scales.count_nonzero()) == 0
+    assert int(out.codes.count_nonzero()) == 0
+    assert_q_equal(out_t, quant.quantize_transpose(f32(x), "rne", rht_seed=1), what="zero transpose")
     assert B.nvfp4_get_status() == B.NVFP4_OK
 
 

@@ -91,6 +91,11 @@ def test_fwht_butterfly_equals_tree_ordered_product():
     tree-ordered sums the oracle defines, bit for bit."""
     rng = np.random.default_rng(2)
     x = (rng.standard_normal((20000, 16)) * np.exp(rng.uniform(-20, 20, (20000, 16)))).astype(np.float32)
+    # exact zeros, signed zeros and exactly cancelling pairs
+    x[:2000] = 0.0
+    x[1000:2000, ::3] = -0.0
+    x[2000:4000, 1::2] = x[2000:4000, 0::2]
+    x[4000:5000, 8:] = -x[4000:5000, :8]
     s = rht.rht_signs(11)
     t = (x * s.astype(np.float32)).astype(np.float32)
     for h in (1, 2, 4, 8):
@@ -101,7 +106,9 @@ def test_fwht_butterfly_equals_tree_ordered_product():
                 t[:, i] = a + b
                 t[:, i + h] = a - b
     t = (t * np.float32(0.25)).astype(np.float32)
+    t = (t + np.float32(0.0)).astype(np.float32)  # an exact zero is +0
     np.testing.assert_array_equal(t.view(np.uint32), rht.rht16_chunks(x, s).view(np.uint32))
+    assert not np.any(np.signbit(rht.rht16_chunks(x, s)) & (rht.rht16_chunks(x, s) == 0))
 
 
 def test_rht_cancels_in_wgrad():
