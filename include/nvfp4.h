@@ -235,6 +235,32 @@ nvfp4_status nvfp4_linear_get_views(void* ws_dev, int64_t M, int64_t K, int64_t 
                                     nvfp4_linear_views* views);
 
 /*
+ * nvfp4_linear_fwd_noalloc -- nvfp4_linear_fwd without a caller workspace.
+ * The paper has no counterpart; this is a convenience of the library.
+ *
+ * Some callers cannot allocate device memory of their own: a plugin inside a
+ * host framework whose allocator owns all of the GPU's memory and forbids
+ * direct cudaMalloc, or a service whose device-memory budget is fixed at
+ * start-up.  This entry point computes the same Y = X W^T as
+ * nvfp4_linear_fwd (same kernels, same results) but takes its workspace from
+ * a 32 MiB array that the library itself holds in device memory, on every GPU
+ * that loads the library, until the process exits.  It allocates nothing.
+ *   x_dev, w_dev, y_dev  as in nvfp4_linear_fwd (the caller still owns them).
+ * Limits: nvfp4_linear_workspace_bytes(M, K, N) must be at most 32 MiB
+ * (33554432 bytes), e.g. M = K = N = 2048; larger layers return
+ * NVFP4_ERR_WORKSPACE before anything is launched.  Other size rules as
+ * nvfp4_linear_fwd.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the one array and leaves its contents behind; nothing in it has
+ * to start at zero.  Calls whose work overlaps on the GPU (other streams, or
+ * other host threads) race on the array: serialise them.  The quantized
+ * operands left in the array are not a valid input for nvfp4_linear_bwd.
+ */
+nvfp4_status nvfp4_linear_fwd_noalloc(const void* x_dev, const void* w_dev, int64_t M, int64_t K, int64_t N,
+                                      uint64_t seed, void* y_dev, nvfp4_stream stream);
+
+/*
  * nvfp4_get_status -- synchronises `stream`, then returns and clears the
  * current device's status word (NVFP4_OK if no device-side error was seen
  * since the last call); NVFP4_ERR_CUDA if the synchronisation failed.

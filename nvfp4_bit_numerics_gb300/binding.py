@@ -42,7 +42,7 @@ NVFP4_OUT_F32 = 1
 EXPORTED = [
     "nvfp4_amax", "nvfp4_quantize", "nvfp4_scale_bytes", "nvfp4_gemm", "nvfp4_linear_workspace_bytes",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_linear_get_views", "nvfp4_get_status",
-    "nvfp4_status_string", "nvfp4_kernel_launch_count",
+    "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
 ]
 
 
@@ -93,6 +93,7 @@ def load_library(path=LIB_PATH):
         "nvfp4_get_status": (I32, [P]),
         "nvfp4_status_string": (ctypes.c_char_p, [I32]),
         "nvfp4_kernel_launch_count": (U64, []),
+        "nvfp4_linear_fwd_noalloc": (I32, [P, P, I64, I64, I64, U64, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -219,6 +220,20 @@ def nvfp4_linear_bwd(dy, K, seed, ws, dx=None, dw=None, stream=None):
     _check("nvfp4_linear_bwd", load_library().nvfp4_linear_bwd(
         _ptr(dy), M, K, N, seed, _ptr(dx), _ptr(dw), _ptr(ws), ws.numel(), _stream(stream)))
     return dx, dw
+
+
+def nvfp4_linear_fwd_noalloc(x, w, seed, y=None, stream=None):
+    """nvfp4_linear_fwd with the library's own 32 MiB device workspace, for
+    callers that must not allocate a workspace (see include/nvfp4.h)."""
+    _bf16_2d(x, "x")
+    _bf16_2d(w, "w")
+    M, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check("nvfp4_linear_fwd_noalloc", load_library().nvfp4_linear_fwd_noalloc(
+        _ptr(x), _ptr(w), M, K, N, seed, _ptr(y), _stream(stream)))
+    return y
 
 
 def nvfp4_linear_get_views(ws, M, K, N):
