@@ -92,19 +92,29 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
   return r;
 }
 
-// Stochastic rounding of one value with a 16-bit uniform u: the lower grid
-// neighbour lo and the spacing give frac = (|v| - lo) / spacing (exact); the
-// value rounds up iff u < frac * 2^16.  |v| >= 6 saturates to 6.
+// Stochastic rounding of one value with a 16-bit uniform u: with lo the
+// lower grid neighbour of |v| and step the grid spacing there,
+// frac = (|v| - lo) / step, and the value rounds up iff u < frac * 2^16.
+// Worked on the float32 bits, exactly:
+//   |v| in [1, 6):   lo keeps the exponent and the top mantissa bit, so frac
+//                    is the 22 lower mantissa bits / 2^22 and the test is
+//                    64 u < those bits; the code is 2(e+1) + top bit + up.
+//   |v| in [.5, 1):  lo = .5, step = .5: frac = 23 mantissa bits / 2^23, the
+//                    test is 128 u < those bits; code 1 + up.
+//   |v| in [0, .5):  lo = 0, step = .5: frac = 2|v|; the test
+//                    u < |v| * 2^17 is exact in float32; code up.
+//   |v| >= 6:        saturates to 6 (code 7).
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u16) {
-  const uint32_t sign = (__float_as_uint(v) >> 31) << 3;
-  const float a = fabsf(v);
-  if (a >= 6.0f) return sign | 7u;
-  const uint32_t idx = (uint32_t)(a >= 0.5f) + (uint32_t)(a >= 1.0f) + (uint32_t)(a >= 1.5f) +
-                       (uint32_t)(a >= 2.0f) + (uint32_t)(a >= 3.0f) + (uint32_t)(a >= 4.0f);
-  const float lo = idx < 4 ? 0.5f * (float)idx : (float)(idx - 2);
-  const float inv_step = idx < 4 ? 2.0f : (idx < 6 ? 1.0f : 0.5f);
-  const float frac = __fmul_rn(__fsub_rn(a, lo), inv_step);
-  return sign | (idx + (uint32_t)((float)u16 < __fmul_rn(frac, 65536.0f)));
+  const uint32_t bits = __float_as_uint(v);
+  const uint32_t a = bits & 0x7FFFFFFFu;
+  // all three candidates, then selects: no data-dependent branches
+  const uint32_t c_hi = 2u * ((a >> 23) - 126u) + ((a >> 22) & 1u) + (uint32_t)((u16 << 6) < (a & 0x3FFFFFu));
+  const uint32_t c_mid = 1u + (uint32_t)((u16 << 7) < (a & 0x7FFFFFu));
+  const uint32_t c_lo = (uint32_t)((float)u16 < __fmul_rn(__uint_as_float(a), 131072.0f));
+  uint32_t code = a >= 0x3F000000u ? c_mid : c_lo;  // 0.5
+  code = a >= 0x3F800000u ? c_hi : code;            // 1.0
+  code = a >= 0x40C00000u ? 7u : code;              // 6.0
+  return ((bits >> 31) << 3) | code;
 }
 
 // ---------------------------------------------------------------------------

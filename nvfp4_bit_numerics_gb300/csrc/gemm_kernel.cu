@@ -11,15 +11,19 @@
 //   warp 0      TMA producer: 2D tiled loads of the packed codes (128-byte
 //               rows, 128B swizzle) and 1D bulk loads of the scale tiles,
 //               into a ring of shared-memory stages guarded by mbarriers.
-//   warp 1      owns the tensor memory; one lane copies each stage's scale
-//               tiles to tensor memory (tcgen05.cp) and issues
+//   warp 1      owns the tensor memory; one lane issues
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X with
 //               the FP32 accumulator in tensor memory, then tcgen05.commit
 //               frees the stage.
-//   warps 2-9   epilogue: tcgen05.ld of the accumulator (each warp reads its
-//               lane quadrant, half of the columns), release the accumulator
-//               to the MMA warp, then scale by ts_a * ts_b, round to BF16 and
-//               store, overlapping the next tile's main loop.
+//   warps 2-5   scale staging: each warp (one per tensor-memory lane
+//               quadrant) copies the stage's scale tiles from shared memory
+//               into that stage's own tensor-memory scale columns with
+//               tcgen05.st, so the tensor pipe runs MMAs only.
+//   warps 6-13  epilogue: tcgen05.ld of the accumulator (each warp reads its
+//               lane quadrant, half of the columns) with scaling by
+//               ts_a * ts_b and BF16 rounding chunk by chunk, release of the
+//               accumulator to the MMA warp, then the stores, overlapping the
+//               next tile's main loop.
 // Every mbarrier wait is bounded (%globaltimer); on expiry the kernel records
 // NVFP4_ERR_TIMEOUT in the status word, drains its own copies and MMAs,
 // frees tensor memory and returns.
@@ -41,8 +45,10 @@ constexpr int kBM = 128;          // rows of A per tile (MMA M)
 constexpr int kBKBytes = 128;     // bytes of K per stage per row = 256 FP4 values
 constexpr int kMmaK = 64;         // FP4 values per MMA
 constexpr int kKPerStage = 256;   // FP4 values per stage
-constexpr int kNumThreads = 320;  // 10 warps
+constexpr int kNumThreads = 448;  // 14 warps
 constexpr int kEpiWarps = 8;
+constexpr int kSfWarps = 4;
+constexpr int kFirstEpiWarp = 6;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 template <int BN>
@@ -52,12 +58,15 @@ struct Cfg {
   static constexpr int kSfaBytes = (kBM / 128) * 4 * 512;
   static constexpr int kSfbBytes = (BN / 128) * 4 * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStages = (220 * 1024) / kStageBytes > 8 ? 8 : (220 * 1024) / kStageBytes;
-  static constexpr int kSfaCol = BN;             // 4 MMAs x 4 columns
-  static constexpr int kSfbCol = BN + 16;        // 4 MMAs x BN/32 columns
-  static constexpr int kTmemCols = (BN + 16 + 4 * (BN / 32)) <= 256 ? 256 : 512;
+  static constexpr int kStagesSmem = (220 * 1024) / kStageBytes > 8 ? 8 : (220 * 1024) / kStageBytes;
+  static constexpr int kStagesTmem = (512 - BN) / (16 + 4 * (BN / 32));
+  static constexpr int kStages = kStagesSmem < kStagesTmem ? kStagesSmem : kStagesTmem;
+  static constexpr int kSfStageCols = 16 + 4 * (BN / 32);
+  static constexpr int kSfaCol = BN;
+  static constexpr int kSfbCol = BN + 16;
+  static constexpr int kTmemCols = 512;
   static constexpr int kEpiCols = BN / 2;        // accumulator columns per epilogue warp
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kStages * kStageBytes + kBarBytes + 1024;
 };
 
@@ -155,20 +164,10 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Descriptor of a 32-row x 16-byte scale tile (no swizzle): 8-row core
-// matrices of 128 contiguous bytes, 128 B apart.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t addr) {
-  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
-
 // Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1), K-major,
 // UE4M3 scales, N >> 3 at bit 17, M >> 4 at bit 24, dense K = 64.
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
@@ -191,6 +190,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
@@ -217,10 +225,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   // barrier slots: full[S], empty[S], tmem_full, tmem_empty, mma_done
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::kStages + s); };
-  const uint32_t tmem_full = bar_base + 8u * (2 * C::kStages);
+  auto sf_bar = [&](int s) { return bar_base + 8u * (2 * C::kStages + s); };
+  const uint32_t tmem_full = bar_base + 8u * (3 * C::kStages);
   const uint32_t tmem_empty = tmem_full + 8u;
   const uint32_t mma_done = tmem_full + 16u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * C::kStages + 3);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -233,6 +242,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sf_bar(s), kSfWarps);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, kEpiWarps);
@@ -301,21 +311,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_after();
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(full_bar(stage), phase, abort, p.status)) { ok = false; break; }
+          if (!mbar_wait(sf_bar(stage), phase, abort, p.status)) { ok = false; break; }
           tc_fence_after();
           const int nk = (ks == k_stages - 1) ? last_nk : 4;
           const uint32_t sa = base + stage * C::kStageBytes;
           const uint32_t sb = sa + C::kABytes;
-          const uint32_t sfa_s = sb + C::kBBytes;
-          const uint32_t sfb_s = sfa_s + C::kSfaBytes;
+          const uint32_t sf_col = tmem + (uint32_t)(stage * C::kSfStageCols);
           for (int j = 0; j < nk; ++j) {
-            tc_cp_sf(tmem + C::kSfaCol + 4 * j, desc_sf(sfa_s + 512 * j));
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              tc_cp_sf(tmem + C::kSfbCol + (BN / 32) * j + 4 * h, desc_sf(sfb_s + h * 2048 + 512 * j));
-          }
-          for (int j = 0; j < nk; ++j) {
-            tc_mma(tmem, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), idesc, tmem + C::kSfaCol + 4 * j,
-                   tmem + C::kSfbCol + (BN / 32) * j, (ks | j) != 0);
+            tc_mma(tmem, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), idesc, sf_col + C::kSfaCol + 4 * j,
+                   sf_col + C::kSfbCol + (BN / 32) * j, (ks | j) != 0);
           }
           tc_commit(empty_bar(stage));
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -329,10 +333,55 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       volatile int never = 0;
       mbar_wait(mma_done, 0, &never, p.status);
     }
+  } else if (warp < kFirstEpiWarp) {
+    // ------------- scale factors: shared memory -> tensor memory -------------
+    // The MMA reads the scales of row r from tensor-memory lane r, column
+    // r/32 of the tile's 4 columns (replicated over the lane quadrants): lane
+    // i, column c of a scale tile holds the c-th word of the 512-byte tile's
+    // 16-byte row i.  Each stage has its own scale columns, so a stage's
+    // columns are rewritten only after its previous MMAs completed (the
+    // producer refills a stage only after the MMA commit freed it).
+    const int q = warp & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      bool ok = true;
+      for (int ks = 0; ks < k_stages; ++ks) {
+        int ready = 0;
+        if (lane == 0) ready = mbar_wait(full_bar(stage), phase, abort, p.status) ? 1 : 0;
+        ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+        if (!ready) { ok = false; break; }
+        const uint8_t* sfa_s = base_ptr + stage * C::kStageBytes + C::kABytes + C::kBBytes;
+        const uint8_t* sfb_s = sfa_s + C::kSfaBytes;
+        uint32_t r[C::kSfStageCols];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sfa_s + 512 * j + 16 * lane);
+          r[4 * j] = w.x; r[4 * j + 1] = w.y; r[4 * j + 2] = w.z; r[4 * j + 3] = w.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            const uint4 w = *reinterpret_cast<const uint4*>(sfb_s + 2048 * h + 512 * j + 16 * lane);
+            const int o = 16 + (BN / 32) * j + 4 * h;
+            r[o] = w.x; r[o + 1] = w.y; r[o + 2] = w.z; r[o + 3] = w.w;
+          }
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::kSfaCol + stage * C::kSfStageCols);
+#pragma unroll
+        for (int c = 0; c < C::kSfStageCols / 16; ++c) tmem_st16(taddr + 16 * c, r + 16 * c);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_bar(stage));
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
   } else {
     // ------------------------------ epilogue ------------------------------
-    const int q = warp & 3;                 // lane quadrant this warp may read
-    const int half = (warp - 2) >> 2;       // which half of the BN columns
+    const int q = warp & 3;
+    const int half = (warp - kFirstEpiWarp) >> 2;
     const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
@@ -343,40 +392,39 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
       if (!ready) break;
       tc_fence_after();
-      uint32_t v[C::kEpiCols];
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(half * C::kEpiCols);
+      const int64_t row = (int64_t)mb * kBM + 32 * q + lane;
+      const int64_t col0 = (int64_t)nb * BN + half * C::kEpiCols;
+      uint32_t packed[C::kEpiCols / 2];
 #pragma unroll
-      for (int c = 0; c < C::kEpiCols / 32; ++c) tmem_ld32(taddr + 32 * c, v + 32 * c);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      for (int c = 0; c < C::kEpiCols / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 32 * c, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (!p.d_f32) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[16 * c + i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[2 * i])),
+                                             __fmul_rn(alpha, __uint_as_float(v[2 * i + 1])));
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0 + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
+                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
+                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
+                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty);
       acc_phase ^= 1u;
-
-      const int64_t row = (int64_t)mb * kBM + 32 * q + lane;
-      const int64_t col0 = (int64_t)nb * BN + half * C::kEpiCols;
       if (!p.d_f32) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.ldd + col0);
 #pragma unroll
-        for (int c = 0; c < C::kEpiCols / 8; ++c) {
-          uint4 o;
-          o.x = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 0])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 1])));
-          o.y = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 2])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 3])));
-          o.z = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 4])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 5])));
-          o.w = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[8 * c + 6])), __fmul_rn(alpha, __uint_as_float(v[8 * c + 7])));
-          dst[c] = o;
-        }
-      } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0);
-#pragma unroll
-        for (int c = 0; c < C::kEpiCols / 4; ++c) {
-          uint4 o;
-          o.x = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 0])));
-          o.y = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 1])));
-          o.z = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 2])));
-          o.w = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * c + 3])));
-          dst[c] = o;
-        }
+        for (int c = 0; c < C::kEpiCols / 8; ++c)
+          dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
       }
     }
   }

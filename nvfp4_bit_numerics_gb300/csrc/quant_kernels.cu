@@ -188,10 +188,14 @@ __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t*
 }
 
 // ---------------------------------------------------------------------------
-// 64x64 tile kernel: one read of x [rows, cols] BF16 into shared memory, then
+// Tile kernel: one read of x [rows, cols] BF16 per 128x64 tile, staged in
+// shared memory, then
 //  - rowwise:    1x16 blocks along cols of x       -> out_row [rows, cols]
 //  - transposed: 1x16 blocks along rows of x (after the optional 16-point
 //                transform along rows)             -> out_t   [cols, rows]
+// Persistent over tiles.  Thread t: rowwise, row t/2 and two 16-element
+// blocks; transposed, the column pair 2(t%32), 2(t%32)+1 over the 16 rows
+// 16(t/32)..16(t/32)+15 (one 32-bit shared-memory word per row).
 // ---------------------------------------------------------------------------
 struct TileOut {
   uint8_t* codes;
@@ -202,56 +206,84 @@ struct TileOut {
   uint32_t stream;
 };
 
-constexpr int kTile = 64;
+constexpr int kTile = 64;       // 2D kernel tile, and the column width of the tile kernel
+constexpr int kTileRows = 128;  // rows (tokens) per tile of the tile kernel
 constexpr int kTilePitch = 72;  // uint16 per smem row: 144 B, conflict-free 16 B row reads
 
 template <bool kRow, bool kT, bool kRHT, bool kSR>
 __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                               int64_t cols, TileOut orow, TileOut ot,
                                                               uint64_t seed, uint32_t* status) {
-  __shared__ __align__(16) uint16_t tile[kTile * kTilePitch];
+  __shared__ __align__(16) uint16_t tile[kTileRows * kTilePitch];
   const int t = threadIdx.x;
   const int64_t tiles_c = cols / kTile;
-  const int64_t tm = blockIdx.x / tiles_c, tc = blockIdx.x - tm * tiles_c;
-  const int64_t m0 = tm * kTile, c0 = tc * kTile;
+  const int64_t n_tiles = ((rows + kTileRows - 1) / kTileRows) * tiles_c;  // rows % 64 == 0
 
   float s_row = 1.0f, s_t = 1.0f;
   if constexpr (kRow) s_row = tensor_prologue(orow.amax, orow.ts, status);
   if constexpr (kT) s_t = tensor_prologue(ot.amax, ot.ts, status);
+  const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
 
-  // load: 64 rows x 8 vectors of 16 B
+  for (int64_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
+    const int64_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
+    const int64_t m0 = tm * kTileRows, c0 = tc * kTile;
+    const int valid = rows - m0 < kTileRows ? (int)(rows - m0) : kTileRows;  // 64 or 128
+    uint4 q[4];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int v = t + k * kThreads;
-    const int row = v >> 3, cv = v & 7;
-    const uint4 q = ldg_nc_v4(x + (m0 + row) * cols + c0 + cv * 8);
-    *reinterpret_cast<uint4*>(&tile[row * kTilePitch + cv * 8]) = q;
-  }
-  __syncthreads();
+    for (int k = 0; k < 4; ++k) {
+      const int v = t + k * kThreads;
+      q[k] = (v >> 3) < valid ? ldg_nc_v4(x + (m0 + (v >> 3)) * cols + c0 + (v & 7) * 8) : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();  // the previous tile's readers are done
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int v = t + k * kThreads;
+      *reinterpret_cast<uint4*>(&tile[(v >> 3) * kTilePitch + (v & 7) * 8]) = q[k];
+    }
+    __syncthreads();
 
-  if constexpr (kRow) {
-    const int r = t >> 2, bc = t & 3;
-    const uint4* sp = reinterpret_cast<const uint4*>(&tile[r * kTilePitch + bc * 16]);
-    float v[16];
-    unpack8(sp[0], v);
-    unpack8(sp[1], v + 8);
-    uint32_t E;
-    const int64_t gr = m0 + r, gc = c0 + bc * 16;
-    const uint2 o = quantize16<kSR>(v, s_row, E, seed, orow.stream, (uint64_t)(gr * cols + gc));
-    *reinterpret_cast<uint2*>(orow.codes + gr * (cols >> 1) + (gc >> 1)) = o;
-    orow.scales[sf_offset(orow.layout, gr, gc >> 4, cols >> 4)] = (uint8_t)E;
-  }
-  if constexpr (kT) {
-    const int c = t & 63, mc = t >> 6;
-    float v[16];
+    if (kRow && (t >> 1) < valid) {
+      const int r = t >> 1, hb = (t & 1) * 2;  // row, first of two blocks
+      const int64_t gr = m0 + r, gc = c0 + hb * 16;
+      uint32_t cw[4], sc = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[(16 * mc + i) * kTilePitch + c] << 16);
-    if constexpr (kRHT) rht16(v, rht_sign_mask(seed));
-    uint32_t E;
-    const int64_t gr = c0 + c, gm = m0 + 16 * mc;  // row / column of the transposed tensor
-    const uint2 o = quantize16<kSR>(v, s_t, E, seed, ot.stream, (uint64_t)(gr * rows + gm));
-    *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = o;
-    ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)E;
+      for (int b = 0; b < 2; ++b) {
+        const uint4* sp = reinterpret_cast<const uint4*>(&tile[r * kTilePitch + (hb + b) * 16]);
+        float v[16];
+        unpack8(sp[0], v);
+        unpack8(sp[1], v + 8);
+        uint32_t E;
+        const uint2 o = quantize16<kSR>(v, s_row, E, seed, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
+        cw[2 * b] = o.x;
+        cw[2 * b + 1] = o.y;
+        sc |= E << (8 * b);
+      }
+      *reinterpret_cast<uint4*>(orow.codes + gr * (cols >> 1) + (gc >> 1)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      *reinterpret_cast<uint16_t*>(orow.scales + sf_offset(orow.layout, gr, gc >> 4, cols >> 4)) = (uint16_t)sc;
+    }
+    if (kT && 16 * (t >> 5) < valid) {
+      const int pc = (t & 31) * 2, ch = t >> 5;
+      float va[16], vb[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(16 * ch + i) * kTilePitch + pc]);
+        va[i] = bf16lo(w);
+        vb[i] = bf16hi(w);
+      }
+      if constexpr (kRHT) {
+        rht16(va, smask);
+        rht16(vb, smask);
+      }
+      const int64_t gm = m0 + 16 * ch;  // column of the transposed tensor
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t gr = c0 + pc + h;  // row of the transposed tensor
+        uint32_t E;
+        const uint2 o = quantize16<kSR>(h ? vb : va, s_t, E, seed, ot.stream, (uint64_t)(gr * rows + gm));
+        *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = o;
+        ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)E;
+      }
+    }
   }
 }
 
@@ -387,9 +419,9 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
   if (out_row) orow = TileOut{out_row->codes, out_row->scales, amax_row, out_row->tensor_scale, out_row->scale_layout,
                               stream_row};
   if (out_t) ot = TileOut{out_t->codes, out_t->scales, amax_t, out_t->tensor_scale, out_t->scale_layout, stream_t};
-  const int64_t tiles = (rows / kTile) * (cols / kTile);
-  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)tiles);
+  const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * (cols / kTile);
+  const int64_t cap = (int64_t)sm_count() * 8;
+  const dim3 grid((unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap));
   uint32_t* status = device_status_ptr();
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   const bool row = out_row != nullptr, tr = out_t != nullptr;

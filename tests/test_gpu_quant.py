@@ -55,13 +55,14 @@ def test_rowwise(shape, rounding, rht, layout):
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("rounding", ["rne", "sr"])
 @pytest.mark.parametrize("rht", [False, True])
-def test_transpose(shape, rounding, rht):
-    if shape[1] % 128:
+@pytest.mark.parametrize("layout", [B.NVFP4_SCALES_MMA, B.NVFP4_SCALES_LINEAR])
+def test_transpose(shape, rounding, rht, layout):
+    if layout == B.NVFP4_SCALES_MMA and shape[1] % 128:
         pytest.skip("MMA layout needs the transposed rows % 128")
     x = outlier_tensor(*shape, seed=3)
     seed = 42
     rnd = B.NVFP4_ROUND_SR if rounding == "sr" else B.NVFP4_ROUND_RNE
-    out, _ = B.nvfp4_quantize(x.cuda(), B.NVFP4_Q_TRANSPOSE, rnd, rht=rht, seed=seed, sr_stream=1)
+    out, _ = B.nvfp4_quantize(x.cuda(), B.NVFP4_Q_TRANSPOSE, rnd, rht=rht, seed=seed, sr_stream=1, layout=layout)
     ref = quant.quantize_transpose(f32(x), rounding, seed=seed, stream_id=1, rht_seed=seed if rht else None)
     assert_q_equal(out, ref, what="transpose %s rht=%s" % (rounding, rht))
 
@@ -79,6 +80,22 @@ def test_fused_rowwise_and_transpose(shape, rounding):
     ref_t = quant.quantize_transpose(xf, rounding, seed=seed, stream_id=1, rht_seed=seed)
     assert_q_equal(out, ref, what="fused rowwise")
     assert_q_equal(out_t, ref_t, what="fused transpose")
+
+
+@pytest.mark.parametrize("shape", [(64, 128), (192, 256), (320, 192)])
+@pytest.mark.parametrize("rounding", ["rne", "sr"])
+def test_fused_ragged_tiles_linear_layout(shape, rounding):
+    """Token counts that end in a half tile (rows % 128 == 64), linear scale
+    layout on both outputs."""
+    x = outlier_tensor(*shape, seed=14)
+    seed = 21
+    rnd = B.NVFP4_ROUND_SR if rounding == "sr" else B.NVFP4_ROUND_RNE
+    out, out_t = B.nvfp4_quantize(x.cuda(), B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, rnd, rht=True, seed=seed, sr_stream=4,
+                                  sr_stream_t=6, layout=B.NVFP4_SCALES_LINEAR)
+    xf = f32(x)
+    assert_q_equal(out, quant.quantize_1d(xf, rounding, seed=seed, stream_id=4), what="ragged rowwise")
+    assert_q_equal(out_t, quant.quantize_transpose(xf, rounding, seed=seed, stream_id=6, rht_seed=seed),
+                   what="ragged transpose")
 
 
 @pytest.mark.parametrize("shape", [(128, 128), (256, 384), (512, 1024), (384, 128)])
