@@ -11,7 +11,9 @@
 //   warp 0      TMA producer: 2D tiled loads of the packed codes (128-byte
 //               rows, 128B swizzle) and 1D bulk loads of the scale tiles,
 //               into a ring of shared-memory stages guarded by mbarriers.
-//   warp 1      owns the tensor memory; one lane issues
+//   warp 1      owns the tensor memory; one lane waits one barrier per stage
+//               (`sf_ready`, raised by the staging warps after the stage's
+//               operands and scales landed), issues
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X with
 //               the FP32 accumulator in tensor memory, then tcgen05.commit
 //               frees the stage.
@@ -120,8 +122,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait: true when the phase with `parity` completed; false if the
 // kernel is aborting or the wait exceeded kTimeoutNs (which starts the abort).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status) {
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -134,6 +135,11 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       }
     }
   }
+}
+
+// Fast path inline (one try_wait); the bounded spin lives out of line.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort, status);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
@@ -226,10 +232,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::kStages + s); };
   auto sf_bar = [&](int s) { return bar_base + 8u * (2 * C::kStages + s); };
-  const uint32_t tmem_full = bar_base + 8u * (3 * C::kStages);
+  auto sf_full_bar = [&](int s) { return bar_base + 8u * (3 * C::kStages + s); };
+  const uint32_t tmem_full = bar_base + 8u * (4 * C::kStages);
   const uint32_t tmem_empty = tmem_full + 8u;
   const uint32_t mma_done = tmem_full + 16u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * C::kStages + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * C::kStages + 3);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -243,6 +250,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sf_bar(s), kSfWarps);
+      mbar_init(sf_full_bar(s), 1);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, kEpiWarps);
@@ -276,17 +284,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
           const int nk = (ks == k_stages - 1) ? last_nk : 4;
           const uint32_t sf_bytes = (uint32_t)nk * 512u;
-          mbar_arrive_expect_tx(full_bar(stage), C::kABytes + C::kBBytes + sf_bytes * (1 + BN / 128));
           const uint32_t sa = base + stage * C::kStageBytes;
-          tma_load_2d(sa, &tmap_a, ks * kBKBytes, mb * kBM, full_bar(stage));
-          tma_load_2d(sa + C::kABytes, &tmap_b, ks * kBKBytes, nb * BN, full_bar(stage));
+          // scale tiles first, on their own barrier: their staging into
+          // tensor memory overlaps the transfer of the operand tiles
+          mbar_arrive_expect_tx(sf_full_bar(stage), sf_bytes * (1 + BN / 128));
           const uint32_t sfa_s = sa + C::kABytes + C::kBBytes;
-          bulk_load(sfa_s, p.sfa + ((int64_t)mb * p.sf_tiles_k + ks * 4) * 512, sf_bytes, full_bar(stage));
+          bulk_load(sfa_s, p.sfa + ((int64_t)mb * p.sf_tiles_k + ks * 4) * 512, sf_bytes, sf_full_bar(stage));
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)
             bulk_load(sfa_s + C::kSfaBytes + h * 2048,
                       p.sfb + ((int64_t)(nb * (BN / 128) + h) * p.sf_tiles_k + ks * 4) * 512, sf_bytes,
-                      full_bar(stage));
+                      sf_full_bar(stage));
+          mbar_arrive_expect_tx(full_bar(stage), C::kABytes + C::kBBytes);
+          tma_load_2d(sa, &tmap_a, ks * kBKBytes, mb * kBM, full_bar(stage));
+          tma_load_2d(sa + C::kABytes, &tmap_b, ks * kBKBytes, nb * BN, full_bar(stage));
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -296,6 +307,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int s = 0; s < C::kStages; ++s)
         if (issued & (1u << s)) {
           volatile int never = 0;
+          mbar_wait(sf_full_bar(s), (issued_phase >> s) & 1u, &never, p.status);
           mbar_wait(full_bar(s), (issued_phase >> s) & 1u, &never, p.status);
         }
     }
@@ -310,16 +322,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort, p.status)) break;
         tc_fence_after();
         for (int ks = 0; ks < k_stages; ++ks) {
-          if (!mbar_wait(full_bar(stage), phase, abort, p.status)) { ok = false; break; }
+          // sf_ready also covers `full`: the staging warps wait for it first
           if (!mbar_wait(sf_bar(stage), phase, abort, p.status)) { ok = false; break; }
           tc_fence_after();
           const int nk = (ks == k_stages - 1) ? last_nk : 4;
           const uint32_t sa = base + stage * C::kStageBytes;
-          const uint32_t sb = sa + C::kABytes;
-          const uint32_t sf_col = tmem + (uint32_t)(stage * C::kSfStageCols);
+          uint64_t da = desc_sw128(sa), db = desc_sw128(sa + C::kABytes);
+          uint32_t sfa = tmem + (uint32_t)(stage * C::kSfStageCols + C::kSfaCol);
+          uint32_t sfb = tmem + (uint32_t)(stage * C::kSfStageCols + C::kSfbCol);
           for (int j = 0; j < nk; ++j) {
-            tc_mma(tmem, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), idesc, sf_col + C::kSfaCol + 4 * j,
-                   sf_col + C::kSfbCol + (BN / 32) * j, (ks | j) != 0);
+            tc_mma(tmem, da, db, idesc, sfa, sfb, (ks | j) != 0);
+            da += 2;  // +32 bytes along K inside the 128-byte swizzle atom
+            db += 2;
+            sfa += 4;
+            sfb += BN / 32;
           }
           tc_commit(empty_bar(stage));
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -340,7 +356,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // i, column c of a scale tile holds the c-th word of the 512-byte tile's
     // 16-byte row i.  Each stage has its own scale columns, so a stage's
     // columns are rewritten only after its previous MMAs completed (the
-    // producer refills a stage only after the MMA commit freed it).
+    // producer refills a stage, scale tiles first, only after the MMA commit
+    // freed it, so `sf_full` of a stage also means its columns are free).
     const int q = warp & 3;
     int stage = 0;
     uint32_t phase = 0;
@@ -348,7 +365,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       for (int ks = 0; ks < k_stages; ++ks) {
         int ready = 0;
-        if (lane == 0) ready = mbar_wait(full_bar(stage), phase, abort, p.status) ? 1 : 0;
+        if (lane == 0)
+          ready = (mbar_wait(sf_full_bar(stage), phase, abort, p.status) &&
+                   mbar_wait(full_bar(stage), phase, abort, p.status)) ? 1 : 0;
         ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
         if (!ready) { ok = false; break; }
         const uint8_t* sfa_s = base_ptr + stage * C::kStageBytes + C::kABytes + C::kBBytes;
@@ -438,6 +457,370 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// CTA-pair kernel: 256 x 256 output tiles, tcgen05.mma.cta_group::2.
+// The two CTAs of a cluster each hold 128 rows of A and 128 of the 256 rows of
+// B in shared memory (same offsets); one MMA issued by the even CTA computes
+// all 256 x 256, each CTA's tensor memory receiving its own 128 rows.  Per SM
+// this halves the MMA instructions and cuts the operand bytes per flop by a
+// third relative to the single-CTA kernel.
+//   warp 0      producer (both CTAs): waits its own `empty` barrier, loads
+//               its A and B halves; the copies signal the even CTA's `full`
+//               barrier, which the even CTA's producer armed for both.
+//   warp 14     scale producer (both CTAs): fills a ring of 8 shared-memory
+//               scale slots ahead of the MMAs, so scale loads are off the
+//               stage-to-stage critical path.
+//   warp 1      even CTA: MMA issuer with one barrier wait per stage
+//               (`sf_ready`, which the even CTA's staging warps arrive on only
+//               after `full`); commits multicast to both CTAs.
+//   warps 2-5   scale staging (both CTAs): global stage g uses the tensor-
+//               memory scale region g % 5; once the MMAs of stage g - 5 (the
+//               region's previous user) committed, copy stage g's scale tiles
+//               (128 rows of A, all 256 rows of B) from their shared-memory
+//               slot into the region, free the slot, and arrive on the even
+//               CTA's `sf_ready` barrier of the region.  The three rings
+//               (6 operand stages, 3 scale slots, 5 scale regions) are
+//               decoupled so the operand ring is as deep as shared memory
+//               allows.
+//   warps 6-13  epilogue (both CTAs) for the CTA's 128 rows; they release
+//               the accumulator with a remote arrive on the even CTA.
+// ---------------------------------------------------------------------------
+constexpr int kPairBN = 256;
+constexpr int kPairABytes = 128 * kBKBytes;  // per CTA
+constexpr int kPairBBytes = 128 * kBKBytes;  // per CTA (half of B)
+constexpr int kPairSfaBytes = 4 * 512;      // this CTA's 128 A rows, 4 MMAs
+constexpr int kPairSfbBytes = 2 * 4 * 512;  // all 256 B rows, 4 MMAs
+constexpr int kPairSfSlotBytes = kPairSfaBytes + kPairSfbBytes;
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr int kPairSfCols = 16 + 4 * (kPairBN / 32);            // tensor-memory scale columns per stage
+constexpr int kPairSfRegions = (512 - kPairBN) / kPairSfCols;     // 5 tensor-memory scale regions
+constexpr int kPairStages = 6;                                    // shared-memory operand stages
+constexpr int kPairSfSlots = 3;                                   // shared-memory scale ring
+constexpr int kPairBarBytes = 512;
+constexpr int kPairSmemBytes =
+    kPairStages * kPairStageBytes + kPairSfSlots * kPairSfSlotBytes + kPairBarBytes + 1024;
+constexpr int kPairThreads = kNumThreads + 32;  // + the scale producer warp
+constexpr int kPairSfProducerWarp = kNumThreads / 32;
+
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on the even CTA's copy of a barrier.  The arrivals that use it
+// follow a completed tensor-memory access (tcgen05.wait::st / wait::ld) and a
+// tcgen05.fence::before_thread_sync, which order that access before the
+// arrive; there is no ordinary memory to release, so the odd CTA uses the
+// relaxed cluster-scope arrive (a cluster-scope release costs ~0.7 us here)
+// and the even CTA its local arrive.
+__device__ __forceinline__ void mbar_arrive_leader(uint32_t local_addr, uint32_t rank) {
+  if (rank == 0) {
+    mbar_arrive(local_addr);
+  } else {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(0));
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(r) : "memory");
+  }
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar) {
+  const uint16_t mask = 3;
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                           Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sf_base = base + kPairStages * kPairStageBytes;
+  const uint8_t* sf_base_ptr = base_ptr + kPairStages * kPairStageBytes;
+  const uint32_t bar_base = sf_base + kPairSfSlots * kPairSfSlotBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kPairStages * kPairStageBytes + kPairSfSlots * kPairSfSlotBytes);
+  // barrier slots: full[S], empty[S], sf_ready[T], sf_full[R], sf_empty[R], tmem_full, tmem_empty, mma_done
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (kPairStages + s); };
+  auto sf_bar = [&](int t) { return bar_base + 8u * (2 * kPairStages + t); };
+  auto sf_full_bar = [&](int r) { return bar_base + 8u * (2 * kPairStages + kPairSfRegions + r); };
+  auto sf_empty_bar = [&](int r) { return bar_base + 8u * (2 * kPairStages + kPairSfRegions + kPairSfSlots + r); };
+  const uint32_t tmem_full = bar_base + 8u * (2 * kPairStages + kPairSfRegions + 2 * kPairSfSlots);
+  const uint32_t tmem_empty = tmem_full + 8u;
+  const uint32_t mma_done = tmem_full + 16u;
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + kPairSfRegions + 2 * kPairSfSlots + 3);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = p.M / 256, num_n = p.N / kPairBN;
+  const int n_tiles = num_m * num_n;
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+  const int k_stages = (p.K + kKPerStage - 1) / kKPerStage;
+  const int last_nk = ((p.K - 1) % kKPerStage) / kMmaK + 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int t = 0; t < kPairSfRegions; ++t) mbar_init(sf_bar(t), 2 * kSfWarps);
+    for (int r = 0; r < kPairSfSlots; ++r) {
+      mbar_init(sf_full_bar(r), 1);
+      mbar_init(sf_empty_bar(r), kSfWarps);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 2 * kEpiWarps);
+    mbar_init(mma_done, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised, tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = pair; tile < n_tiles; tile += num_pairs) {
+        const int mb = tile % num_m, nb = tile / num_m;
+        bool ok = true;
+        for (int ks = 0; ks < k_stages; ++ks) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
+          const uint32_t sa = base + stage * kPairStageBytes;
+          const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * (kPairABytes + kPairBBytes));
+          tma_load_2d_pair(sa, &tmap_a, ks * kBKBytes, mb * 256 + (int)rank * 128, leader_full);
+          tma_load_2d_pair(sa + kPairABytes, &tmap_b, ks * kBKBytes, nb * kPairBN + (int)rank * 128, leader_full);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == kPairSfProducerWarp) {
+    // ------------------------------ scale producer ------------------------
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t sphase = 0;
+      for (int tile = pair; tile < n_tiles; tile += num_pairs) {
+        const int mb = tile % num_m, nb = tile / num_m;
+        bool ok = true;
+        for (int ks = 0; ks < k_stages; ++ks) {
+          if (!mbar_wait(sf_empty_bar(slot), sphase ^ 1u, abort, p.status)) { ok = false; break; }
+          const int nk = (ks == k_stages - 1) ? last_nk : 4;
+          const uint32_t sf_bytes = (uint32_t)nk * 512u;
+          const uint32_t dst = sf_base + slot * kPairSfSlotBytes;
+          mbar_arrive_expect_tx(sf_full_bar(slot), 3u * sf_bytes);
+          bulk_load(dst, p.sfa + ((int64_t)(2 * mb + (int)rank) * p.sf_tiles_k + ks * 4) * 512, sf_bytes,
+                    sf_full_bar(slot));
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            bulk_load(dst + kPairSfaBytes + h * 2048, p.sfb + ((int64_t)(2 * nb + h) * p.sf_tiles_k + ks * 4) * 512,
+                      sf_bytes, sf_full_bar(slot));
+          if (++slot == kPairSfSlots) { slot = 0; sphase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer (even CTA) ------------------
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc = idesc_mxf4nvf4(256, kPairBN);
+      int stage = 0, region = 0;
+      uint32_t phase = 0, rphase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < n_tiles && ok; tile += num_pairs) {
+        if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort, p.status)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < k_stages; ++ks) {
+          // sf_ready also covers `full`: the even CTA's staging warps wait for it
+          if (!mbar_wait(sf_bar(region), rphase, abort, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const int nk = (ks == k_stages - 1) ? last_nk : 4;
+          const uint32_t sa = base + stage * kPairStageBytes;
+          uint64_t da = desc_sw128(sa), db = desc_sw128(sa + kPairABytes);
+          uint32_t sfa = tmem + (uint32_t)(kPairBN + region * kPairSfCols), sfb = sfa + 16;
+          for (int j = 0; j < nk; ++j) {
+            tc_mma_pair(tmem, da, db, idesc, sfa, sfb, (ks | j) != 0);
+            da += 2;  // +32 bytes along K inside the 128-byte swizzle atom
+            db += 2;
+            sfa += 4;
+            sfb += kPairBN / 32;
+          }
+          tc_commit_pair_multicast(empty_bar(stage));
+          if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+          if (++region == kPairSfRegions) { region = 0; rphase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(tmem_full);
+        acc_phase ^= 1u;
+      }
+      tc_commit_pair(mma_done);
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, p.status);
+    }
+  } else if (warp < kFirstEpiWarp) {
+    // ---------------- scale factors: shared memory -> tensor memory -------------
+    // Same replicated layout as the single-CTA kernel: lane i, column c of a
+    // scale tile holds the c-th word of the 512-byte tile's 16-byte row i.
+    // A stage's columns are rewritten only after that stage's previous MMAs
+    // committed (`empty`); the shared-memory slot is freed after the copy.
+    const int q = warp & 3;
+    int g = 0, stage = 0, slot = 0, region = 0;
+    uint32_t phase = 0, sphase = 0, rphase = 0;
+    for (int tile = pair; tile < n_tiles; tile += num_pairs) {
+      bool ok = true;
+      for (int ks = 0; ks < k_stages; ++ks, ++g) {
+        int ready = 0;
+        if (lane == 0) {
+          // the region's previous user is stage g - 5: operand stage
+          // (g - 5) % 6, committed in round (g - 5) / 6
+          const int gp = g - kPairSfRegions;
+          ready = (mbar_wait(sf_full_bar(slot), sphase, abort, p.status) &&
+                   (gp < 0 || mbar_wait(empty_bar(gp % kPairStages), (uint32_t)(gp / kPairStages) & 1u, abort,
+                                        p.status)) &&
+                   (rank != 0 || mbar_wait(full_bar(stage), phase, abort, p.status))) ? 1 : 0;
+        }
+        ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+        if (!ready) { ok = false; break; }
+        tc_fence_after();
+        const uint8_t* sfa_s = sf_base_ptr + slot * kPairSfSlotBytes;
+        const uint8_t* sfb_s = sfa_s + kPairSfaBytes;
+        uint32_t r[kPairSfCols];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 wa = *reinterpret_cast<const uint4*>(sfa_s + 512 * j + 16 * lane);
+          const uint4 w0 = *reinterpret_cast<const uint4*>(sfb_s + 512 * j + 16 * lane);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(sfb_s + 2048 + 512 * j + 16 * lane);
+          r[4 * j] = wa.x; r[4 * j + 1] = wa.y; r[4 * j + 2] = wa.z; r[4 * j + 3] = wa.w;
+          const int o = 16 + 8 * j;
+          r[o] = w0.x; r[o + 1] = w0.y; r[o + 2] = w0.z; r[o + 3] = w0.w;
+          r[o + 4] = w1.x; r[o + 5] = w1.y; r[o + 6] = w1.z; r[o + 7] = w1.w;
+        }
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kPairBN + region * kPairSfCols);
+#pragma unroll
+        for (int c = 0; c < kPairSfCols / 16; ++c) tmem_st16(taddr + 16 * c, r + 16 * c);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(sf_empty_bar(slot));
+          mbar_arrive_leader(sf_bar(region), rank);
+        }
+        if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+        if (++slot == kPairSfSlots) { slot = 0; sphase ^= 1u; }
+        if (++region == kPairSfRegions) { region = 0; rphase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;
+    const int half = (warp - kFirstEpiWarp) >> 2;
+    constexpr int kCols = kPairBN / 2;
+    const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < n_tiles; tile += num_pairs) {
+      const int mb = tile % num_m, nb = tile / num_m;
+      int ready = 0;
+      if (lane == 0) ready = mbar_wait(tmem_full, acc_phase, abort, p.status) ? 1 : 0;
+      ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+      if (!ready) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(half * kCols);
+      const int64_t row = (int64_t)mb * 256 + (int64_t)rank * 128 + 32 * q + lane;
+      const int64_t col0 = (int64_t)nb * kPairBN + half * kCols;
+      uint32_t packed[kCols / 2];
+#pragma unroll
+      for (int c = 0; c < kCols / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 32 * c, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (!p.d_f32) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[16 * c + i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[2 * i])),
+                                             __fmul_rn(alpha, __uint_as_float(v[2 * i + 1])));
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0 + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
+                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
+                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
+                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_leader(tmem_empty, rank);
+      acc_phase ^= 1u;
+      if (!p.d_f32) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.ldd + col0);
+#pragma unroll
+        for (int c = 0; c < kCols / 8; ++c)
+          dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+      }
+    }
+  }
+
+  // Both CTAs stay until every MMA (which reads both CTAs' shared memory) is
+  // done and both epilogues have read their accumulators.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -519,10 +902,49 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+
+nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
+                      cudaStream_t s) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) !=
+        cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  CUtensorMap ma, mb;
+  const int64_t K = a.cols;
+  if (!make_code_map(&ma, a.codes, (uint64_t)K / 2, (uint64_t)a.rows, 128) ||
+      !make_code_map(&mb, b.codes, (uint64_t)K / 2, (uint64_t)b.rows, 128))
+    return NVFP4_ERR_CUDA;
+  Params p;
+  p.sfa = a.scales;
+  p.sfb = b.scales;
+  p.ts_a = a.tensor_scale;
+  p.ts_b = b.tensor_scale;
+  p.d = d;
+  p.ldd = ldd;
+  p.d_f32 = d_dtype == NVFP4_OUT_F32;
+  p.M = (int)a.rows;
+  p.N = (int)b.rows;
+  p.K = (int)K;
+  p.sf_tiles_k = (int)(K / 64);
+  p.status = device_status_ptr();
+  const int tiles = (p.M / 256) * (p.N / kPairBN);
+  const int pairs_max = sm_count() / 2;
+  const int pairs = tiles < pairs_max ? tiles : pairs_max;
+  nvfp4_gemm_pair_kernel<<<2 * pairs, kPairThreads, kPairSmemBytes, s>>>(ma, mb, p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 }  // namespace
 
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
                          cudaStream_t s) {
+  if (a.rows % 256 == 0 && b.rows % 256 == 0) return run_pair(a, b, d, d_dtype, ldd, s);
   if (b.rows % 256 == 0) return run<256>(a, b, d, d_dtype, ldd, s);
   return run<128>(a, b, d, d_dtype, ldd, s);
 }

@@ -90,6 +90,7 @@ def test_random_gemm(M, N, K):
     qa, qb = make_q(ac, asc, ta), make_q(bc, bsc, tb)
     ref = ref_gemm(ac, asc, ta, bc, bsc, tb)
     d32 = B.nvfp4_gemm(qa, qb, out_dtype=torch.float32).cpu().numpy()
+    assert B.nvfp4_get_status() == B.NVFP4_OK
     assert rel_fro(d32, ref) <= 1e-5
     d16 = B.nvfp4_gemm(qa, qb).float().cpu().numpy()
     assert rel_fro(d16, formats.float64_to_bf16_rne(ref)) <= 1e-3
