@@ -323,7 +323,7 @@ def run_gpu(args, rank, world, local):
                          "bytes": "2 reads of BF16 dY (amax, quantize) + 2 x 0.5625 B/elem written"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp4_peak, "traffic": traffic_record(),
-                     "kernel": "nvfp4_gemm_kernel<256> (mean of Fprop, Dgrad, Wgrad)",
+                     "kernel": "nvfp4_gemm_pair_kernel (mean of Fprop, Dgrad, Wgrad)",
                      "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:BF16)" % (src, bf16,
                                                                                          FP4_OVER_BF16)},
         "e2e": {"value": FLOPS_PER_STEP * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -82,8 +82,22 @@ struct Params {
   int d_f32;
   int M, N, K;
   int sf_tiles_k;  // 4-scale tiles per 128-row scale tile row = K / 64
+  int n_fastest;   // tile order: 1 = consecutive tiles walk N (B stays in L2)
   uint32_t* status;
 };
+
+// Tile index -> (m block, n block).  Consecutive tiles (which run at the same
+// time on neighbouring SMs) walk the dimension whose operand is the smaller,
+// so that operand stays resident in L2 while the larger one streams once.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int n_fastest, int& mb, int& nb) {
+  if (n_fastest) {
+    nb = tile % num_n;
+    mb = tile / num_n;
+  } else {
+    mb = tile % num_m;
+    nb = tile / num_m;
+  }
+}
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -279,7 +293,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t issued = 0, issued_phase = 0;  // per-stage bits, for the drain
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int mb = tile % num_m, nb = tile / num_m;
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
           const int nk = (ks == k_stages - 1) ? last_nk : 4;
@@ -404,7 +419,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-      const int mb = tile % num_m, nb = tile / num_m;
+      int mb, nb;
+        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
       // one lane waits, the warp follows its verdict (tcgen05.ld is warp-wide)
       int ready = 0;
       if (lane == 0) ready = mbar_wait(tmem_full, acc_phase, abort, p.status) ? 1 : 0;
@@ -628,7 +644,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = pair; tile < n_tiles; tile += num_pairs) {
-        const int mb = tile % num_m, nb = tile / num_m;
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
         bool ok = true;
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
@@ -648,7 +665,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int slot = 0;
       uint32_t sphase = 0;
       for (int tile = pair; tile < n_tiles; tile += num_pairs) {
-        const int mb = tile % num_m, nb = tile / num_m;
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
         bool ok = true;
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(sf_empty_bar(slot), sphase ^ 1u, abort, p.status)) { ok = false; break; }
@@ -766,7 +784,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < n_tiles; tile += num_pairs) {
-      const int mb = tile % num_m, nb = tile / num_m;
+      int mb, nb;
+        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
       int ready = 0;
       if (lane == 0) ready = mbar_wait(tmem_full, acc_phase, abort, p.status) ? 1 : 0;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
@@ -894,6 +913,7 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
   p.N = (int)b.rows;
   p.K = (int)K;
   p.sf_tiles_k = (int)(K / 64);
+  p.n_fastest = p.N < p.M;
   p.status = device_status_ptr();
   const int tiles = (p.M / kBM) * (p.N / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
@@ -931,6 +951,7 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   p.N = (int)b.rows;
   p.K = (int)K;
   p.sf_tiles_k = (int)(K / 64);
+  p.n_fastest = p.N < p.M;
   p.status = device_status_ptr();
   const int tiles = (p.M / 256) * (p.N / kPairBN);
   const int pairs_max = sm_count() / 2;
