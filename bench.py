@@ -46,6 +46,24 @@ def dist_info():
     return rank, world, local
 
 
+def reduce_max_over_ranks(x, world, device=None):
+    """Max of a per-rank scalar over all ranks (the slowest rank sets the step
+    time); a no-op on one rank."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(ms_per_step, world):
+    """Weak scaling: every rank runs one full layer step per step."""
+    return FLOPS_PER_STEP * world / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -254,13 +272,7 @@ def run_gpu(args, rank, world, local):
 
     part = np.array([[marks[i][j].elapsed_time(marks[i][j + 1]) for j in range(6)] for i in range(args.steps)])
     gemm_ms = float(np.mean(part[:, [2, 4, 5]]))
-    ms_per_step = total_ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = reduce_max_over_ranks(total_ms / args.steps, world, dev)
 
     # e2e: the public layer API on pinned host buffers, copies inside the region
     xp, wp, dyp = (t.pin_memory() for t in (x_h, w_h, dy_h))
@@ -287,13 +299,7 @@ def run_gpu(args, rank, world, local):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (x_h, w_h, dy_h))
     d2h = sum(t.numel() * t.element_size() for t in (yp, dxp, dwp))
 
@@ -308,7 +314,7 @@ def run_gpu(args, rank, world, local):
     q_bytes = dy_elems * (2 + 2 + 2 * 0.5625)
     q_ms = float(np.mean(part[:, 3]))
     cpu_s, cpu_flops = cpu_oracle_step(*(workloads.bf16_to_f32_numpy(t) for t in (x_h, w_h, dy_h)))
-    value = FLOPS_PER_STEP * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(ms_per_step, world)
     line = {
         "metric": "NVFP4 linear fwd+bwd TFLOPS", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -326,7 +332,7 @@ def run_gpu(args, rank, world, local):
                      "kernel": "nvfp4_gemm_pair_kernel (mean of Fprop, Dgrad, Wgrad)",
                      "peak_source": "%s bf16 burst %.1f TFLOP/s x %.0f (nominal FP4:BF16)" % (src, bf16,
                                                                                          FP4_OVER_BF16)},
-        "e2e": {"value": FLOPS_PER_STEP * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": whole_job_tflops(e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "api": "nvfp4_linear_fwd + nvfp4_linear_bwd"},
         "gpu_launches": int(launches),

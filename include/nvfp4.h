@@ -271,6 +271,17 @@ const char* nvfp4_status_string(nvfp4_status status);
 /* Number of kernels this library launched since load (host-side count). */
 uint64_t nvfp4_kernel_launch_count(void);
 
+/*
+ * nvfp4_debug_stall_next_gemm -- failure-detection test hook (no counterpart
+ * in the paper).  With on != 0, the next nvfp4_gemm launch never issues the
+ * loads of its first pipeline stage, so every pipeline wait of that launch
+ * runs into its bound (about 2 s): the kernel stops its roles, frees its
+ * tensor memory and returns, nvfp4_get_status then reports
+ * NVFP4_ERR_TIMEOUT, and the CUDA context stays usable.  The output of that
+ * launch is unspecified.  The flag applies to one launch only.
+ */
+void nvfp4_debug_stall_next_gemm(int32_t on);
+
 #ifdef __cplusplus
 }
 #endif

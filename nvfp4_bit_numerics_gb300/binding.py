@@ -43,6 +43,7 @@ EXPORTED = [
     "nvfp4_amax", "nvfp4_quantize", "nvfp4_scale_bytes", "nvfp4_gemm", "nvfp4_linear_workspace_bytes",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_linear_get_views", "nvfp4_get_status",
     "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
+    "nvfp4_debug_stall_next_gemm",
 ]
 
 
@@ -94,6 +95,7 @@ def load_library(path=LIB_PATH):
         "nvfp4_status_string": (ctypes.c_char_p, [I32]),
         "nvfp4_kernel_launch_count": (U64, []),
         "nvfp4_linear_fwd_noalloc": (I32, [P, P, I64, I64, I64, U64, P, P]),
+        "nvfp4_debug_stall_next_gemm": (None, [I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -257,6 +259,10 @@ def nvfp4_linear_get_views(ws, M, K, N):
 def nvfp4_get_status(stream=None):
     """Synchronises the stream; returns and clears the device status code."""
     return int(load_library().nvfp4_get_status(_stream(stream)))
+
+
+def nvfp4_debug_stall_next_gemm(on=True):
+    load_library().nvfp4_debug_stall_next_gemm(1 if on else 0)
 
 
 def nvfp4_kernel_launch_count():

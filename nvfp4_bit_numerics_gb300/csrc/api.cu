@@ -82,6 +82,8 @@ const char* nvfp4_status_string(nvfp4_status s) {
 
 uint64_t nvfp4_kernel_launch_count(void) { return g_launches.load(); }
 
+void nvfp4_debug_stall_next_gemm(int32_t on) { set_gemm_debug_stall(on); }
+
 nvfp4_status nvfp4_get_status(nvfp4_stream stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
   uint32_t w = 0;

@@ -35,6 +35,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -83,6 +84,7 @@ struct Params {
   int M, N, K;
   int sf_tiles_k;  // 4-scale tiles per 128-row scale tile row = K / 64
   int n_fastest;   // tile order: 1 = consecutive tiles walk N (B stays in L2)
+  int debug_stall; // failure-detection test: the first stage's loads are never issued
   uint32_t* status;
 };
 
@@ -297,6 +299,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
+          if (p.debug_stall && tile == (int)blockIdx.x && ks == 0) {
+            // nothing is issued or armed for this stage: the consumers' bounded
+            // waits run out and the kernel reports NVFP4_ERR_TIMEOUT
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           const int nk = (ks == k_stages - 1) ? last_nk : 4;
           const uint32_t sf_bytes = (uint32_t)nk * 512u;
           const uint32_t sa = base + stage * C::kStageBytes;
@@ -649,6 +657,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         bool ok = true;
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
+          if (p.debug_stall && tile == pair && ks == 0) {
+            // nothing is issued or armed for this stage: the consumers' bounded
+            // waits run out and the kernel reports NVFP4_ERR_TIMEOUT
+            if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           const uint32_t sa = base + stage * kPairStageBytes;
           const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * (kPairABytes + kPairBBytes));
@@ -843,6 +857,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+std::atomic<int> g_debug_stall{0};
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -914,6 +930,7 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
   p.K = (int)K;
   p.sf_tiles_k = (int)(K / 64);
   p.n_fastest = p.N < p.M;
+  p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
   const int tiles = (p.M / kBM) * (p.N / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
@@ -952,6 +969,7 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   p.K = (int)K;
   p.sf_tiles_k = (int)(K / 64);
   p.n_fastest = p.N < p.M;
+  p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
   const int tiles = (p.M / 256) * (p.N / kPairBN);
   const int pairs_max = sm_count() / 2;
@@ -962,6 +980,8 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
 }
 
 }  // namespace
+
+void set_gemm_debug_stall(int on) { g_debug_stall.store(on ? 1 : 0); }
 
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
                          cudaStream_t s) {

@@ -41,6 +41,10 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
 cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvfp4_tensor& out,
                             const nvfp4_tensor* out_t, const float* amax, cudaStream_t s);
 
+// Failure-detection test hook: the next GEMM launch never issues its first
+// stage's loads, so its bounded waits run out (gemm_kernel.cu).
+void set_gemm_debug_stall(int on);
+
 // GEMM launcher (gemm_kernel.cu).  Arguments are already validated.
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
                          cudaStream_t s);

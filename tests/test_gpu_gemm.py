@@ -124,3 +124,70 @@ def test_gemm_repeatable():
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert B.nvfp4_get_status() == B.NVFP4_OK
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (128, 384, 512)])
+def test_pipeline_wait_bound_reports_timeout(M, N, K):
+    """Failure detection without a GPU fault: the test hook makes one launch
+    skip its first stage's loads, so the pipeline waits run out (about 2 s),
+    the kernel stops and reports NVFP4_ERR_TIMEOUT, and the next GEMM on the
+    same context is correct.  (256x512: CTA-pair kernel; 128x384: 1-CTA.)"""
+    import time
+
+    rng = np.random.default_rng(9)
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    asc = rng.integers(0x30, 0x40, size=(M, K // 16)).astype(np.uint8)
+    bsc = rng.integers(0x30, 0x40, size=(N, K // 16)).astype(np.uint8)
+    qa, qb = make_q(ac, asc, 1.0), make_q(bc, bsc, 1.0)
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    B.nvfp4_debug_stall_next_gemm(True)
+    t0 = time.time()
+    B.nvfp4_gemm(qa, qb)
+    st = B.nvfp4_get_status()
+    dt = time.time() - t0
+    assert st == B.NVFP4_ERR_TIMEOUT
+    assert 1.0 < dt < 30.0
+    d = B.nvfp4_gemm(qa, qb, out_dtype=torch.float32).cpu().numpy()
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    assert rel_fro(d, ref_gemm(ac, asc, 1.0, bc, bsc, 1.0)) <= 1e-5
+
+
+@pytest.mark.parametrize("K,N,w2d,rht", [(4096, 4096, True, False), (5120, 5120, False, True),
+                                         (20480, 5120, True, False)])
+def test_gemm_sweep_full_size_sampled(K, N, w2d, rht):
+    """The GEMM shape sweep at full size (M = 16384, heavy-tailed X ~ t(3),
+    W ~ N(0, 0.02)): X quantized 1x16, W with 16x16 blocks or 1x16, with or
+    without the Hadamard transform along K on both operands; sampled rows of
+    the output against the oracle."""
+    from nvfp4_bit_numerics_gb300 import workloads
+    from tests.gpu_util import assert_q_equal, f32
+
+    x, w, _ = workloads.gemm_sweep(K, N)
+    M = x.shape[0]
+    xf, wf = f32(x), f32(w)
+    seed = 4
+    qx, _ = B.nvfp4_quantize(x.cuda(), B.NVFP4_Q_ROWWISE, rht=rht, seed=seed)
+    if w2d:
+        qw, _ = B.nvfp4_quantize(w.cuda(), B.NVFP4_Q_2D)
+    else:
+        qw, _ = B.nvfp4_quantize(w.cuda(), B.NVFP4_Q_ROWWISE, rht=rht, seed=seed)
+    d = B.nvfp4_gemm(qx, qw)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(2).choice(M, 8, replace=False))
+    ax = quant.amax_rht(xf, seed, axis=1) if rht else quant.tensor_amax(xf)
+    rx = quant.quantize_1d(xf, "rne", rht_seed=seed if rht else None, amax=ax, row_ids=rows)
+    assert_q_equal(qx, rx, rows=rows, what="X")
+    if w2d:
+        r2 = quant.quantize_2d(wf)
+        rw = dict(codes=r2["codes"], scales=r2["scales"], amax=r2["amax"], ts=r2["ts"])
+    else:
+        rw = quant.quantize_1d(wf, "rne", rht_seed=seed if rht else None)
+    assert_q_equal(qw, rw, what="W")
+    ref = gemm.gemm_ref(rx["codes"], rx["scales"], rx["ts"], rw["codes"], rw["scales"], rw["ts"])
+    got = d[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert rel_fro(got, formats.float64_to_bf16_rne(ref)) <= 1e-3
+    if rht:
+        # the transform cancels: the product is close to the unquantized X W^T
+        exact = xf[rows].astype(np.float64) @ wf.astype(np.float64).T
+        assert rel_fro(got, exact) < 0.15

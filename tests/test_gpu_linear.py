@@ -67,15 +67,17 @@ def test_layer_step_is_deterministic():
         assert torch.equal(a, b)
 
 
-def test_mlp_up_full_size_sampled():
-    """The MLP up-projection layer at full size (M=8192, K=5120, N=20480),
-    launched exactly as the benchmark launches it.  The oracle recomputes the
-    amaxes and the quantized operands it needs and the GEMM outputs of
-    sampled rows of Y, dX and dW."""
-    x, w, dy = workloads.mlp_up()
+@pytest.mark.parametrize("layer", ["mlp_up", "mlp_down", "qkv"])
+def test_layer_full_size_sampled(layer):
+    """The full-size layers: MLP up-projection (M=8192, K=5120, N=20480, the
+    benchmark's workload, launched as the benchmark launches it), MLP
+    down-projection (K=20480, N=5120) and the QKV projection (K=5120,
+    N=7168).  The oracle recomputes the amaxes and the quantized operands it
+    needs and the GEMM outputs of sampled rows of Y, dX and dW."""
+    x, w, dy = getattr(workloads, layer)()
     M, K = x.shape
     N = w.shape[0]
-    seed = 2
+    seed = 2 if layer == "mlp_up" else 3
     y, dx, dw, v = run_layer(x, w, dy, seed)
     xf, wf, dyf = f32(x), f32(w), f32(dy)
     rng = np.random.default_rng(1)
