@@ -288,66 +288,130 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
 }
 
 // ---------------------------------------------------------------------------
-// 2D weight quantization, 64x64 tile = 4x4 blocks of 16x16.  Thread t holds
-// row t/4, block column t%4 (16 elements).  Writes W's codes directly and
-// W^T's codes through a shared-memory transpose of the 4-bit codes.
+// 2D weight quantization: persistent over 64 x 128 tiles (4 x 8 blocks of
+// 16 x 16) staged in shared memory.
+//  - block pass: thread (br, bc, rp) holds rows rp and rp + 8 of block (br, bc);
+//    the block amax is a shuffle over the 8 threads of the block; it encodes
+//    its two rows (W codes, K-major).
+//  - column pass: thread (br, column pair) encodes the 16 x 2 column slice of
+//    its block with the same block scale (W^T codes, N-major).  Encoding an
+//    element twice gives the same code, so W^T is exactly W transposed.
+//  - scales: one 32-bit store per 4 blocks of a row of W and of W^T.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) quant_2d_kernel(const uint16_t* __restrict__ w, int64_t rows,
+constexpr int k2dRows = 64, k2dCols = 128;
+constexpr int k2dPitch = 136;  // uint16 per smem row: 272 B
+
+__global__ void __launch_bounds__(kThreads, 4) quant_2d_kernel(const uint16_t* __restrict__ w, int64_t rows,
                                                             int64_t cols, const float* amax, TileOut ow,
                                                             TileOut owt, int has_t, uint32_t* status) {
-  __shared__ uint32_t s_amax[8][4];
-  __shared__ uint32_t s_E[4][4];
-  __shared__ uint8_t s_codes[kTile][kTile];
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int64_t tiles_c = cols / kTile;
-  const int64_t tm = blockIdx.x / tiles_c, tc = blockIdx.x - tm * tiles_c;
-  const int64_t r0 = tm * kTile, c0 = tc * kTile;
-  const float s_enc = tensor_prologue(amax, ow.ts, status);
-  if (has_t && blockIdx.x == 0 && t == 0) *owt.ts = tensor_decode_scale(s_enc);
+  __shared__ __align__(16) uint16_t tile[k2dRows * k2dPitch];
+  __shared__ float s_enc[4][8];
+  __shared__ uint32_t s_E[4][8];
+  const int t = threadIdx.x;
+  const float s_tensor = tensor_prologue(amax, ow.ts, status);
+  if (has_t && blockIdx.x == 0 && t == 0) *owt.ts = tensor_decode_scale(s_tensor);
+  const int64_t tiles_c = (cols + k2dCols - 1) / k2dCols;  // cols % 64 == 0
+  const int64_t n_tiles = (rows / k2dRows) * tiles_c;
+  const int br = t >> 6, bc = (t >> 3) & 7, rp = t & 7;
 
-  const int r = t >> 2, bc = t & 3;
-  const uint16_t* p = w + (r0 + r) * cols + c0 + bc * 16;
-  float v[16];
-  unpack8(ldg_nc_v4(p), v);
-  unpack8(ldg_nc_v4(p + 8), v + 8);
-  uint32_t m = 0;
+  // the next tile's loads are issued before the current tile is processed
+  uint4 q[4];
+  auto load_tile = [&](int64_t tl) {
+    const int64_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
+    const int64_t r0 = tm * k2dRows, c0 = tc * k2dCols;
+    const int valid_cols = cols - c0 < k2dCols ? (int)(cols - c0) : k2dCols;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) m = max(m, abs_bits(v[i]));
-  // lanes 4r'+bc of this warp hold rows 8*warp + r' of block column bc
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-  if (lane < 4) s_amax[warp][lane] = m;
-  __syncthreads();
-  const int br = r >> 4;
-  const uint32_t mb = max(s_amax[2 * br][bc], s_amax[2 * br + 1][bc]);
-  uint32_t E;
-  float enc;
-  block_scale(__uint_as_float(mb), s_enc, E, enc);
-  float s[16];
+    for (int k = 0; k < 4; ++k) {
+      const int v = t + k * kThreads;  // 64 rows x 16 vectors
+      const int row = v >> 4, cv = v & 15;
+      q[k] = cv * 8 < valid_cols ? ldg_nc_v4(w + (r0 + row) * cols + c0 + cv * 8) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  if (blockIdx.x < n_tiles) load_tile(blockIdx.x);
+  for (int64_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
+    const int64_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
+    const int64_t r0 = tm * k2dRows, c0 = tc * k2dCols;
+    const int valid_cols = cols - c0 < k2dCols ? (int)(cols - c0) : k2dCols;  // 64 or 128
+    __syncthreads();  // the previous tile's readers are done
 #pragma unroll
-  for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(v[i], enc);
-  const uint32_t lo = e2m1x8_rn(s), hi = e2m1x8_rn(s + 8);
-  const int64_t gr = r0 + r, gc = c0 + bc * 16;
-  *reinterpret_cast<uint2*>(ow.codes + gr * (cols >> 1) + (gc >> 1)) = make_uint2(lo, hi);
-  ow.scales[sf_offset(ow.layout, gr, gc >> 4, cols >> 4)] = (uint8_t)E;
-  if (!has_t) return;
+    for (int k = 0; k < 4; ++k) {
+      const int v = t + k * kThreads;
+      *reinterpret_cast<uint4*>(&tile[(v >> 4) * k2dPitch + (v & 15) * 8]) = q[k];
+    }
+    __syncthreads();
+    if (tl + gridDim.x < n_tiles) load_tile(tl + gridDim.x);
 
+    // ---- block pass: amax, scale, W codes
+    const bool col_ok = bc * 16 < valid_cols;
+    float v[32];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    s_codes[r][bc * 16 + i] = (lo >> (4 * i)) & 15u;
-    s_codes[r][bc * 16 + 8 + i] = (hi >> (4 * i)) & 15u;
+    for (int h = 0; h < 2; ++h) {
+      const uint4* sp = reinterpret_cast<const uint4*>(&tile[(16 * br + rp + 8 * h) * k2dPitch + bc * 16]);
+      unpack8(sp[0], v + 16 * h);
+      unpack8(sp[1], v + 16 * h + 8);
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = max(m, abs_bits(v[i]));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    uint32_t E;
+    float enc;
+    block_scale(__uint_as_float(m), s_tensor, E, enc);
+    if (rp == 0) {
+      s_E[br][bc] = E;
+      s_enc[br][bc] = enc;
+    }
+    if (col_ok) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float sv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sv[i] = __fmul_rn(v[16 * h + i], enc);
+        const int64_t gr = r0 + 16 * br + rp + 8 * h, gc = c0 + bc * 16;
+        *reinterpret_cast<uint2*>(ow.codes + gr * (cols >> 1) + (gc >> 1)) =
+            make_uint2(e2m1x8_rn(sv), e2m1x8_rn(sv + 8));
+      }
+    }
+    __syncthreads();
+
+    // ---- scales: W rows (4 blocks per store), W^T rows (4 block rows per store)
+    if (t < 128) {
+      const int row = t >> 1, g = t & 1;
+      if (g * 64 < valid_cols) {
+        const int b = row >> 4;
+        const uint32_t w4 = s_E[b][4 * g] | (s_E[b][4 * g + 1] << 8) | (s_E[b][4 * g + 2] << 16) |
+                            (s_E[b][4 * g + 3] << 24);
+        *reinterpret_cast<uint32_t*>(ow.scales + sf_offset(ow.layout, r0 + row, (c0 >> 4) + 4 * g, cols >> 4)) =
+            w4;
+      }
+    } else if (has_t && t - 128 < valid_cols) {
+      const int k = t - 128, b = k >> 4;
+      const uint32_t w4 = s_E[0][b] | (s_E[1][b] << 8) | (s_E[2][b] << 16) | (s_E[3][b] << 24);
+      *reinterpret_cast<uint32_t*>(owt.scales + sf_offset(owt.layout, c0 + k, r0 >> 4, rows >> 4)) = w4;
+    }
+    if (!has_t) continue;
+
+    // ---- column pass: W^T codes
+    {
+      const int cp = t & 63, bcc = cp >> 3;
+      if (bcc * 16 < valid_cols) {
+        float va[16], vb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t wd = *reinterpret_cast<const uint32_t*>(&tile[(16 * br + i) * k2dPitch + 2 * cp]);
+          va[i] = __fmul_rn(bf16lo(wd), s_enc[br][bcc]);
+          vb[i] = __fmul_rn(bf16hi(wd), s_enc[br][bcc]);
+        }
+        const int64_t tcol = r0 + 16 * br;
+        const int64_t tr = c0 + 2 * cp;
+        *reinterpret_cast<uint2*>(owt.codes + tr * (rows >> 1) + (tcol >> 1)) = make_uint2(e2m1x8_rn(va), e2m1x8_rn(va + 8));
+        *reinterpret_cast<uint2*>(owt.codes + (tr + 1) * (rows >> 1) + (tcol >> 1)) =
+            make_uint2(e2m1x8_rn(vb), e2m1x8_rn(vb + 8));
+      }
+    }
   }
-  if ((r & 15) == 0) s_E[br][bc] = E;
-  __syncthreads();
-  // thread t -> row k = t/4 of the W^T tile (column k of W), chunk nc = t%4
-  const int k = t >> 2, nc = t & 3;
-  uint32_t tw[2] = {0u, 0u};
-#pragma unroll
-  for (int i = 0; i < 16; ++i) tw[i >> 3] |= (uint32_t)s_codes[16 * nc + i][k] << (4 * (i & 7));
-  const int64_t tr = c0 + k, tcol = r0 + 16 * nc;
-  *reinterpret_cast<uint2*>(owt.codes + tr * (rows >> 1) + (tcol >> 1)) = make_uint2(tw[0], tw[1]);
-  owt.scales[sf_offset(owt.layout, tr, tcol >> 4, rows >> 4)] = (uint8_t)s_E[nc][k >> 4];
 }
 
 }  // namespace
@@ -445,10 +509,11 @@ cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvf
   TileOut ow{out.codes, out.scales, amax, out.tensor_scale, out.scale_layout, 0};
   TileOut owt{};
   if (out_t) owt = TileOut{out_t->codes, out_t->scales, amax, out_t->tensor_scale, out_t->scale_layout, 0};
-  const int64_t tiles = (rows / kTile) * (cols / kTile);
-  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  quant_2d_kernel<<<(unsigned)tiles, kThreads, 0, s>>>(static_cast<const uint16_t*>(w), rows, cols, amax, ow, owt,
-                                                       out_t ? 1 : 0, device_status_ptr());
+  const int64_t tiles = (rows / k2dRows) * ((cols + k2dCols - 1) / k2dCols);
+  const int64_t cap = (int64_t)sm_count() * 8;
+  const unsigned grid = (unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
+  quant_2d_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(w), rows, cols, amax, ow, owt,
+                                            out_t ? 1 : 0, device_status_ptr());
   count_launch();
   return cudaGetLastError();
 }

@@ -98,10 +98,11 @@ def test_fused_ragged_tiles_linear_layout(shape, rounding):
                    what="ragged transpose")
 
 
-@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (512, 1024), (384, 128)])
+@pytest.mark.parametrize("shape", [(128, 128), (256, 384), (512, 1024), (384, 128), (128, 192), (64, 64)])
 def test_quant_2d(shape):
     w = outlier_tensor(*shape, seed=5, sigma=0.02)
-    out, out_t = B.nvfp4_quantize(w.cuda(), B.NVFP4_Q_2D)
+    layout = B.NVFP4_SCALES_MMA if shape[0] % 128 == 0 and shape[1] % 128 == 0 else B.NVFP4_SCALES_LINEAR
+    out, out_t = B.nvfp4_quantize(w.cuda(), B.NVFP4_Q_2D, layout=layout)
     ref = quant.quantize_2d(f32(w))
     assert_q_equal(out, dict(codes=ref["codes"], scales=ref["scales"], amax=ref["amax"], ts=ref["ts"]), what="W")
     assert_q_equal(out_t, dict(codes=ref["codes_t"], scales=ref["scales_t"], amax=ref["amax"], ts=ref["ts"]),
