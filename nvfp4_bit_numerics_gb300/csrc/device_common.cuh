@@ -95,26 +95,27 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
 // Stochastic rounding of one value with a 16-bit uniform u: with lo the
 // lower grid neighbour of |v| and step the grid spacing there,
 // frac = (|v| - lo) / step, and the value rounds up iff u < frac * 2^16.
-// Worked on the float32 bits, exactly:
-//   |v| in [1, 6):   lo keeps the exponent and the top mantissa bit, so frac
-//                    is the 22 lower mantissa bits / 2^22 and the test is
-//                    64 u < those bits; the code is 2(e+1) + top bit + up.
-//   |v| in [.5, 1):  lo = .5, step = .5: frac = 23 mantissa bits / 2^23, the
-//                    test is 128 u < those bits; code 1 + up.
-//   |v| in [0, .5):  lo = 0, step = .5: frac = 2|v|; the test
-//                    u < |v| * 2^17 is exact in float32; code up.
-//   |v| >= 6:        saturates to 6 (code 7).
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u16) {
-  const uint32_t bits = __float_as_uint(v);
-  const uint32_t a = bits & 0x7FFFFFFFu;
-  // all three candidates, then selects: no data-dependent branches
-  const uint32_t c_hi = 2u * ((a >> 23) - 126u) + ((a >> 22) & 1u) + (uint32_t)((u16 << 6) < (a & 0x3FFFFFu));
-  const uint32_t c_mid = 1u + (uint32_t)((u16 << 7) < (a & 0x7FFFFFu));
-  const uint32_t c_lo = (uint32_t)((float)u16 < __fmul_rn(__uint_as_float(a), 131072.0f));
-  uint32_t code = a >= 0x3F000000u ? c_mid : c_lo;  // 0.5
-  code = a >= 0x3F800000u ? c_hi : code;            // 1.0
-  code = a >= 0x40C00000u ? 7u : code;              // 6.0
-  return ((bits >> 31) << 3) | code;
+// The result is the rounded grid value with the sign of v (cvt then gives
+// its code exactly).  The caller passes nu = 2^22 - 1 - 64 u.
+//   |v| in [1, 6]:  lo keeps the exponent and the top mantissa bit of |v|,
+//                   and frac * 2^22 is the integer m of the lower 22 mantissa
+//                   bits.  64 u < m  <=>  m + nu >= 2^22: adding nu to the
+//                   bits carries into bit 22 exactly when the value rounds
+//                   up, and clearing the lower 22 bits leaves lo or its upper
+//                   neighbour (a carry out of the mantissa steps the
+//                   exponent, which is the next grid point as well).
+//   |v| in [0, 1):  the grid 0, .5, 1 is 1, 1.5, 2 shifted by one.  x =
+//                   RU(|v| + 1) has lower 22 mantissa bits ceil(frac * 2^22),
+//                   and for an integer n, n < y <=> n < ceil(y), so the same
+//                   carry test on x decides exactly; 1 is subtracted after
+//                   (exact).
+//   |v| >= 6, NaN:  fminf gives 6, which no nu moves (code 7).
+__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t nu) {
+  const float av = fabsf(v);
+  const float off = av < 1.0f ? 1.0f : 0.0f;
+  const float x = fminf(__fadd_ru(av, off), 6.0f);
+  const float r = __uint_as_float((__float_as_uint(x) + nu) & 0xFFC00000u);
+  return __uint_as_float(__float_as_uint(__fsub_rn(r, off)) | (__float_as_uint(v) & 0x80000000u));
 }
 
 // ---------------------------------------------------------------------------
@@ -133,25 +134,27 @@ __device__ __forceinline__ u32x4 philox4x32_10(u32x4 c, uint32_t k0, uint32_t k1
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = u32x4{hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0};
+    const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u, p1 = (uint64_t)c.z * 0xCD9E8D57u;
+    c = u32x4{(uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0};
   }
   return c;
 }
 
-// The 16 uniforms of 16 consecutive elements starting at e0 (e0 % 8 == 0):
-// two Philox calls with counters (e0/8, e0/8 + 1), low half first.
-__device__ __forceinline__ void sr_uniforms16(uint64_t seed, uint32_t stream, uint64_t e0, uint32_t* u) {
+// The stochastic-rounding inputs nu = 2^22 - 1 - 64 u of 16 consecutive
+// elements starting at e0 (e0 % 8 == 0): their uniforms u come from two
+// Philox calls with counters (e0/8, e0/8 + 1), low half of each word first.
+__device__ __forceinline__ void sr_nu16(uint64_t seed, uint32_t stream, uint64_t e0, uint32_t* nu) {
   const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint64_t g = (e0 >> 3) + h;
     const u32x4 w = philox4x32_10(u32x4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, k0, k1);
-    u[8 * h + 0] = w.x & 0xFFFFu; u[8 * h + 1] = w.x >> 16;
-    u[8 * h + 2] = w.y & 0xFFFFu; u[8 * h + 3] = w.y >> 16;
-    u[8 * h + 4] = w.z & 0xFFFFu; u[8 * h + 5] = w.z >> 16;
-    u[8 * h + 6] = w.w & 0xFFFFu; u[8 * h + 7] = w.w >> 16;
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      nu[8 * h + 2 * j] = 0x3FFFFFu - ((ws[j] & 0xFFFFu) << 6);
+      nu[8 * h + 2 * j + 1] = 0x3FFFFFu - ((ws[j] >> 16) << 6);
+    }
   }
 }
 
@@ -200,21 +203,16 @@ __device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, uint32_
   float s[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(v[i], enc);
-  uint2 out;
-  if constexpr (!kSR) {
-    out.x = e2m1x8_rn(s);
-    out.y = e2m1x8_rn(s + 8);
-  } else {
-    uint32_t u[16];
-    sr_uniforms16(seed, stream, e0, u);
-    uint32_t lo = 0, hi = 0;
+  if constexpr (kSR) {
+    uint32_t nu[16];
+    sr_nu16(seed, stream, e0, nu);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) lo |= e2m1_sr(s[i], u[i]) << (4 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) hi |= e2m1_sr(s[8 + i], u[8 + i]) << (4 * i);
-    out.x = lo;
-    out.y = hi;
+    for (int i = 0; i < 16; ++i) s[i] = e2m1_sr_value(s[i], nu[i]);
   }
+  // RNE here, or the exact conversion of grid values after SR
+  uint2 out;
+  out.x = e2m1x8_rn(s);
+  out.y = e2m1x8_rn(s + 8);
   return out;
 }
 
