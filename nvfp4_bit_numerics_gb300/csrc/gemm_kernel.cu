@@ -85,6 +85,7 @@ struct Params {
   int sf_tiles_k;  // 4-scale tiles per 128-row scale tile row = K / 64
   int n_fastest;   // tile order: 1 = consecutive tiles walk N (B stays in L2)
   int debug_stall; // failure-detection test: the first stage's loads are never issued
+  int tma_store;   // pair kernel: BF16 output written by bulk tensor stores
   uint32_t* status;
 };
 
@@ -508,7 +509,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //               decoupled so the operand ring is as deep as shared memory
 //               allows.
 //   warps 6-13  epilogue (both CTAs) for the CTA's 128 rows; they release
-//               the accumulator with a remote arrive on the even CTA.
+//               the accumulator with a remote arrive on the even CTA, then
+//               write BF16 output as 32-row x 16-column boxes staged in a
+//               1 KB shared-memory buffer per warp and sent with bulk tensor
+//               stores.  (Per-lane 16-byte global stores -- 32 rows per warp
+//               instruction -- flooded the memory pipeline at every tile
+//               boundary and held up the barrier traffic of the main loop.)
 // ---------------------------------------------------------------------------
 constexpr int kPairBN = 256;
 constexpr int kPairABytes = 128 * kBKBytes;  // per CTA
@@ -521,9 +527,10 @@ constexpr int kPairSfCols = 16 + 4 * (kPairBN / 32);            // tensor-memory
 constexpr int kPairSfRegions = (512 - kPairBN) / kPairSfCols;     // 5 tensor-memory scale regions
 constexpr int kPairStages = 6;                                    // shared-memory operand stages
 constexpr int kPairSfSlots = 3;                                   // shared-memory scale ring
+constexpr int kPairEpiBufBytes = 1024;                            // per epilogue warp: 32 rows x 16 BF16
 constexpr int kPairBarBytes = 512;
-constexpr int kPairSmemBytes =
-    kPairStages * kPairStageBytes + kPairSfSlots * kPairSfSlotBytes + kPairBarBytes + 1024;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kPairSfSlots * kPairSfSlotBytes +
+                               kEpiWarps * kPairEpiBufBytes + kPairBarBytes + 1024;
 constexpr int kPairThreads = kNumThreads + 32;  // + the scale producer warp
 constexpr int kPairSfProducerWarp = kNumThreads / 32;
 
@@ -547,6 +554,16 @@ __device__ __forceinline__ void mbar_arrive_leader(uint32_t local_addr, uint32_t
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(0));
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(r) : "memory");
   }
+}
+
+// Bulk tensor store of a shared-memory box, tracked in the issuing thread's
+// bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -585,15 +602,16 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                           Params p) {
+                           const __grid_constant__ CUtensorMap tmap_d, Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t sf_base = base + kPairStages * kPairStageBytes;
   const uint8_t* sf_base_ptr = base_ptr + kPairStages * kPairStageBytes;
-  const uint32_t bar_base = sf_base + kPairSfSlots * kPairSfSlotBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kPairStages * kPairStageBytes + kPairSfSlots * kPairSfSlotBytes);
+  const uint32_t epi_base = sf_base + kPairSfSlots * kPairSfSlotBytes;
+  const uint32_t bar_base = epi_base + kEpiWarps * kPairEpiBufBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + (bar_base - base));
   // barrier slots: full[S], empty[S], sf_ready[T], sf_full[R], sf_empty[R], tmem_full, tmem_empty, mma_done
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (kPairStages + s); };
@@ -833,13 +851,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_leader(tmem_empty, rank);
       acc_phase ^= 1u;
-      if (!p.d_f32) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.ldd + col0);
+      if (p.tma_store) {
+        // 16-column chunks through this warp's 1 KB buffer: 32 rows of 32 B,
+        // 32-byte swizzle (16-byte half h of row r at h ^ bit 2 of r), one
+        // bulk tensor store per chunk; the buffer is rewritten once the
+        // previous store has read it.
+        const uint32_t buf = epi_base + (uint32_t)(warp - kFirstEpiWarp) * kPairEpiBufBytes;
+        const uint32_t sw = (uint32_t)((lane >> 2) & 1);
 #pragma unroll
-        for (int c = 0; c < kCols / 8; ++c)
-          dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        for (int j = 0; j < kCols / 16; ++j) {
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t a = buf + (uint32_t)lane * 32u + (((uint32_t)h ^ sw) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(packed[8 * j + 4 * h]),
+                         "r"(packed[8 * j + 4 * h + 1]), "r"(packed[8 * j + 4 * h + 2]), "r"(packed[8 * j + 4 * h + 3])
+                         : "memory");
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&tmap_d, (int)col0 + 16 * j, (int)(row - lane), buf);
+        }
       }
     }
+    // the output is in global memory (and the buffers free) before exit
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   // Both CTAs stay until every MMA (which reads both CTAs' shared memory) is
@@ -883,6 +920,20 @@ bool make_code_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D map over a BF16 [rows, cols] output with row stride ld elements; box =
+// 16 columns x 32 rows, 32-byte swizzle (the epilogue's staging layout).
+bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -932,6 +983,7 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
   p.n_fastest = p.N < p.M;
   p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
+  p.tma_store = 0;
   const int tiles = (p.M / kBM) * (p.N / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
   nvfp4_gemm_kernel<BN><<<grid, kNumThreads, C::kSmemBytes, s>>>(ma, mb, p);
@@ -971,10 +1023,15 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   p.n_fastest = p.N < p.M;
   p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
+  // BF16 output goes through bulk tensor stores (the API guarantees the
+  // 16-byte aligned base and row stride they need); FP32 through plain stores
+  CUtensorMap md = ma;  // unused for FP32 output
+  p.tma_store = !p.d_f32;
+  if (p.tma_store && !make_out_map(&md, d, (uint64_t)p.N, (uint64_t)p.M, (uint64_t)ldd)) return NVFP4_ERR_CUDA;
   const int tiles = (p.M / 256) * (p.N / kPairBN);
   const int pairs_max = sm_count() / 2;
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
-  nvfp4_gemm_pair_kernel<<<2 * pairs, kPairThreads, kPairSmemBytes, s>>>(ma, mb, p);
+  nvfp4_gemm_pair_kernel<<<2 * pairs, kPairThreads, kPairSmemBytes, s>>>(ma, mb, md, p);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -111,6 +111,26 @@ def test_strided_output():
     assert rel_fro(o[:, :N], ref_gemm(ac, asc, 1.0, bc, bsc, 1.0)) <= 1e-5
 
 
+@pytest.mark.parametrize("pad", [0, 8, 136])
+def test_strided_bf16_output_pair_kernel(pad):
+    """BF16 output with a row stride on the CTA-pair kernel (M, N multiples
+    of 256), whose epilogue writes 16-column boxes with bulk tensor stores:
+    the padding columns stay untouched and every value matches."""
+    rng = np.random.default_rng(5 + pad)
+    M, N, K = 512, 768, 512
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    sc = lambda r: rng.integers(0x30, 0x40, size=(r, K // 16)).astype(np.uint8)
+    asc, bsc = sc(M), sc(N)
+    out = torch.full((M, N + pad), 7.0, dtype=torch.bfloat16, device="cuda")
+    B.nvfp4_gemm(make_q(ac, asc, 0.5), make_q(bc, bsc, 2.0), out=out[:, :N])
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    o = out.float().cpu().numpy()
+    assert np.all(o[:, N:] == 7.0)
+    ref = formats.float64_to_bf16_rne(ref_gemm(ac, asc, 0.5, bc, bsc, 2.0))
+    assert rel_fro(o[:, :N], ref) <= 1e-3
+
+
 def test_gemm_repeatable():
     rng = np.random.default_rng(4)
     M, N, K = 256, 512, 768
