@@ -505,9 +505,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //               (128 rows of A, all 256 rows of B) from their shared-memory
 //               slot into the region, free the slot, and arrive on the even
 //               CTA's `sf_ready` barrier of the region.  The three rings
-//               (6 operand stages, 3 scale slots, 5 scale regions) are
+//               (6 operand stages, 4 scale slots, 5 scale regions) are
 //               decoupled so the operand ring is as deep as shared memory
-//               allows.
+//               allows.  A scale load is issued when its slot is freed by
+//               the staging of the stage 4 earlier and lands ~1 us later, so
+//               the slot count bounds the staging rate at about
+//               (load latency + staging time) / slots per stage: with 3
+//               slots that, not the tensor pipe, set the main-loop pace.
 //   warps 6-13  epilogue (both CTAs) for the CTA's 128 rows; they release
 //               the accumulator with a remote arrive on the even CTA, then
 //               write BF16 output as 32-row x 16-column boxes staged in a
@@ -526,11 +530,12 @@ constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairSfCols = 16 + 4 * (kPairBN / 32);            // tensor-memory scale columns per stage
 constexpr int kPairSfRegions = (512 - kPairBN) / kPairSfCols;     // 5 tensor-memory scale regions
 constexpr int kPairStages = 6;                                    // shared-memory operand stages
-constexpr int kPairSfSlots = 3;                                   // shared-memory scale ring
+constexpr int kPairSfSlots = 4;                                   // shared-memory scale ring
 constexpr int kPairEpiBufBytes = 1024;                            // per epilogue warp: 32 rows x 16 BF16
 constexpr int kPairBarBytes = 512;
 constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kPairSfSlots * kPairSfSlotBytes +
                                kEpiWarps * kPairEpiBufBytes + kPairBarBytes + 1024;
+static_assert(kPairSmemBytes <= 232448, "pair kernel shared memory exceeds the 227 KB opt-in limit");
 constexpr int kPairThreads = kNumThreads + 32;  // + the scale producer warp
 constexpr int kPairSfProducerWarp = kNumThreads / 32;
 
