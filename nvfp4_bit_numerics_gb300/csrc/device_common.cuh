@@ -65,12 +65,37 @@ __device__ __forceinline__ float tensor_encode_scale(float amax) {
 }
 __device__ __forceinline__ float tensor_decode_scale(float s_enc) { return __fdiv_rn(1.0f, s_enc); }
 
+// fl(a / 6) for a >= 0.  From 2^-120 up, q = fl(a * fl(1/6)) corrected by
+// one FMA on the exact remainder a - 6q is the correctly rounded quotient
+// (checked against a double-precision division for every float in
+// [2^-120, inf)); below, where a / 6 nears the subnormal range, the IEEE
+// division itself.
+__device__ __forceinline__ float div6_rn(float a) {
+  if (a < 0x1p-120f) return __fdiv_rn(a, 6.0f);
+  const float r6 = 1.0f / 6.0f;
+  const float q = __fmul_rn(a, r6);
+  return __fmaf_rn(__fmaf_rn(-q, 6.0f, a), r6, q);
+}
+
 // Block scale from the block amax: E = e4m3(fl(fl(amax_b / 6) * s_enc)),
 // enc = fl(s_enc / e4m3(E)) or 0 when E == 0.
 __device__ __forceinline__ void block_scale(float amax_b, float s_enc, uint32_t& E, float& enc) {
-  const float sd = __fdiv_rn(amax_b, 6.0f);
-  E = e4m3_rn_satfinite(__fmul_rn(sd, s_enc));
+  E = e4m3_rn_satfinite(__fmul_rn(div6_rn(amax_b), s_enc));
   enc = E ? __fdiv_rn(s_enc, e4m3_value(E)) : 0.0f;
+}
+
+// enc of every E4M3 code for one tensor (128 entries; codes 0 and 0x7F,
+// which never occurs under satfinite, hold 0); the thread with index i in
+// [0, 128) fills entry i, other indices do nothing.
+__device__ __forceinline__ void fill_enc_table(float* tab, float s_enc, int i) {
+  if (i >= 0 && i < 128) tab[i] = (i == 0 || i == 0x7F) ? 0.0f : __fdiv_rn(s_enc, e4m3_value((uint32_t)i));
+}
+
+// block_scale with enc taken from the tensor's table.
+__device__ __forceinline__ void block_scale_tab(float amax_b, float s_enc, const float* tab, uint32_t& E,
+                                                float& enc) {
+  E = e4m3_rn_satfinite(__fmul_rn(div6_rn(amax_b), s_enc));
+  enc = tab[E];
 }
 
 // ---------------------------------------------------------------------------
@@ -95,9 +120,10 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
 // Stochastic rounding of one value with a 16-bit uniform u: with lo the
 // lower grid neighbour of |v| and step the grid spacing there,
 // frac = (|v| - lo) / step, and the value rounds up iff u < frac * 2^16.
-// The result is the rounded grid value with the sign of v (cvt then gives
-// its code exactly).  The caller passes nu = 2^22 - 1 - 64 u.
-//   |v| in [1, 6]:  lo keeps the exponent and the top mantissa bit of |v|,
+// The result is the rounded grid value with the sign of v, or for |v| > 6 a
+// value at least 6, which the saturating conversion to E2M1 turns into 6
+// (code 7).  The caller passes nu = 2^22 - 1 - 64 u.
+//   |v| in [1, 8):  lo keeps the exponent and the top mantissa bit of |v|,
 //                   and frac * 2^22 is the integer m of the lower 22 mantissa
 //                   bits.  64 u < m  <=>  m + nu >= 2^22: adding nu to the
 //                   bits carries into bit 22 exactly when the value rounds
@@ -108,12 +134,14 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
 //                   RU(|v| + 1) has lower 22 mantissa bits ceil(frac * 2^22),
 //                   and for an integer n, n < y <=> n < ceil(y), so the same
 //                   carry test on x decides exactly; 1 is subtracted after
-//                   (exact).
-//   |v| >= 6, NaN:  fminf gives 6, which no nu moves (code 7).
+//                   (exact).  The shift, 1 below 1 and 0 from 1 up, is one
+//                   saturating FMA: sat(2^126 (1 - |v|)).
+//   |v| >= 8:       the truncated value stays >= 8 and saturates to 6.
+// Non-finite inputs (which the amax pass reports) give unspecified codes.
 __device__ __forceinline__ float e2m1_sr_value(float v, uint32_t nu) {
   const float av = fabsf(v);
-  const float off = av < 1.0f ? 1.0f : 0.0f;
-  const float x = fminf(__fadd_ru(av, off), 6.0f);
+  const float off = __saturatef(__fmaf_rn(-av, 0x1p126f, 0x1p126f));
+  const float x = __fadd_ru(av, off);
   const float r = __uint_as_float((__float_as_uint(x) + nu) & 0xFFC00000u);
   return __uint_as_float(__float_as_uint(__fsub_rn(r, off)) | (__float_as_uint(v) & 0x80000000u));
 }
@@ -185,21 +213,28 @@ __device__ __forceinline__ void rht16(float* v, uint32_t sign_mask) {
       }
     }
   }
+  // v * 0.25 + 0 in one rounding: equal to the product rounded and then
+  // +0 added except where v / 4 underflows to zero (|v| <= 2^-148), which
+  // sums of BF16 values (multiples of 2^-133) never reach.
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(__fmul_rn(v[j], 0.25f), 0.0f);
+  for (int j = 0; j < 16; ++j) v[j] = __fmaf_rn(v[j], 0.25f, 0.0f);
 }
 
 // ---------------------------------------------------------------------------
 // One 1x16 block: amax_b, scale, 16 codes -> (8 code bytes as uint2, E)
 // ---------------------------------------------------------------------------
+// enc_tab: the tensor's table of fill_enc_table.
 template <bool kSR>
-__device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, uint32_t& E, uint64_t seed,
-                                            uint32_t stream, uint64_t e0) {
-  uint32_t m = 0;
+__device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, const float* enc_tab, uint32_t& E,
+                                            uint64_t seed, uint32_t stream, uint64_t e0) {
+  // block amax as a float max of |v| (the absolute value is an operand
+  // modifier); equal to the bit-pattern max for finite values, and the
+  // tensor's amax pass already reports non-finite input
+  float m = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) m = max(m, abs_bits(v[i]));
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
   float enc;
-  block_scale(__uint_as_float(m), s_enc, E, enc);
+  block_scale_tab(m, s_enc, enc_tab, E, enc);
   float s[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(v[i], enc);

@@ -155,6 +155,9 @@ __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t*
                                                                  uint8_t* scales, int layout, float* ts_out,
                                                                  uint64_t seed, uint32_t stream, uint32_t* status) {
   const float s_enc = tensor_prologue(amax, ts_out, status);
+  __shared__ float enc_tab[128];
+  fill_enc_table(enc_tab, s_enc, threadIdx.x);
+  __syncthreads();
   const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
   const int64_t gpr = cols >> 6;  // 64-element groups per row
   const int64_t units = rows * gpr;
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t*
       unpack8(q[2 * b + 1], v + 8);
       if constexpr (kRHT) rht16(v, smask);
       uint32_t E;
-      const uint2 o = quantize16<kSR>(v, s_enc, E, seed, stream, (uint64_t)(r * cols + c0 + 16 * b));
+      const uint2 o = quantize16<kSR>(v, s_enc, enc_tab, E, seed, stream, (uint64_t)(r * cols + c0 + 16 * b));
       cw[2 * b] = o.x;
       cw[2 * b + 1] = o.y;
       sc |= E << (8 * b);
@@ -222,6 +225,11 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
   float s_row = 1.0f, s_t = 1.0f;
   if constexpr (kRow) s_row = tensor_prologue(orow.amax, orow.ts, status);
   if constexpr (kT) s_t = tensor_prologue(ot.amax, ot.ts, status);
+  // enc tables (rowwise tensor, transposed tensor); the first tile's
+  // __syncthreads orders them before use
+  __shared__ float enc_tab[2][128];
+  if constexpr (kRow) fill_enc_table(enc_tab[0], s_row, t);
+  if constexpr (kT) fill_enc_table(enc_tab[1], s_t, t - 128);
   const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
 
   for (int64_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
@@ -253,7 +261,8 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
         unpack8(sp[0], v);
         unpack8(sp[1], v + 8);
         uint32_t E;
-        const uint2 o = quantize16<kSR>(v, s_row, E, seed, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
+        const uint2 o =
+            quantize16<kSR>(v, s_row, enc_tab[0], E, seed, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
         cw[2 * b] = o.x;
         cw[2 * b + 1] = o.y;
         sc |= E << (8 * b);
@@ -279,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
       for (int h = 0; h < 2; ++h) {
         const int64_t gr = c0 + pc + h;  // row of the transposed tensor
         uint32_t E;
-        const uint2 o = quantize16<kSR>(h ? vb : va, s_t, E, seed, ot.stream, (uint64_t)(gr * rows + gm));
+        const uint2 o = quantize16<kSR>(h ? vb : va, s_t, enc_tab[1], E, seed, ot.stream, (uint64_t)(gr * rows + gm));
         *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = o;
         ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)E;
       }
