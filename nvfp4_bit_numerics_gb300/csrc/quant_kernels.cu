@@ -304,16 +304,20 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
 //    its two rows (W codes, K-major).
 //  - column pass: thread (br, column pair) encodes the 16 x 2 column slice of
 //    its block with the same block scale (W^T codes, N-major).  Encoding an
-//    element twice gives the same code, so W^T is exactly W transposed.
+//    element twice gives the same code, so W^T is exactly W transposed.  The
+//    W^T codes of the tile (128 rows of 32 bytes) are collected in shared
+//    memory and written as one 16-byte store per thread, whole sectors per
+//    row, instead of 8-byte pieces of 64 rows per warp instruction.
 //  - scales: one 32-bit store per 4 blocks of a row of W and of W^T.
 // ---------------------------------------------------------------------------
 constexpr int k2dRows = 64, k2dCols = 128;
 constexpr int k2dPitch = 136;  // uint16 per smem row: 272 B
 
-__global__ void __launch_bounds__(kThreads, 4) quant_2d_kernel(const uint16_t* __restrict__ w, int64_t rows,
+__global__ void __launch_bounds__(kThreads, 3) quant_2d_kernel(const uint16_t* __restrict__ w, int64_t rows,
                                                             int64_t cols, const float* amax, TileOut ow,
                                                             TileOut owt, int has_t, uint32_t* status) {
   __shared__ __align__(16) uint16_t tile[k2dRows * k2dPitch];
+  __shared__ __align__(16) uint2 tbuf[4][k2dCols];  // W^T codes: [block row][W^T row of the tile]
   __shared__ float s_enc[4][8];
   __shared__ uint32_t s_E[4][8];
   const int t = threadIdx.x;
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 4) quant_2d_kernel(const uint16_t* _
     }
     if (!has_t) continue;
 
-    // ---- column pass: W^T codes
+    // ---- column pass: W^T codes, collected per tile, then whole rows
     {
       const int cp = t & 63, bcc = cp >> 3;
       if (bcc * 16 < valid_cols) {
@@ -413,11 +417,16 @@ __global__ void __launch_bounds__(kThreads, 4) quant_2d_kernel(const uint16_t* _
           va[i] = __fmul_rn(bf16lo(wd), s_enc[br][bcc]);
           vb[i] = __fmul_rn(bf16hi(wd), s_enc[br][bcc]);
         }
-        const int64_t tcol = r0 + 16 * br;
-        const int64_t tr = c0 + 2 * cp;
-        *reinterpret_cast<uint2*>(owt.codes + tr * (rows >> 1) + (tcol >> 1)) = make_uint2(e2m1x8_rn(va), e2m1x8_rn(va + 8));
-        *reinterpret_cast<uint2*>(owt.codes + (tr + 1) * (rows >> 1) + (tcol >> 1)) =
-            make_uint2(e2m1x8_rn(vb), e2m1x8_rn(vb + 8));
+        tbuf[br][2 * cp] = make_uint2(e2m1x8_rn(va), e2m1x8_rn(va + 8));
+        tbuf[br][2 * cp + 1] = make_uint2(e2m1x8_rn(vb), e2m1x8_rn(vb + 8));
+      }
+      __syncthreads();
+      // thread t: W^T row t / 2 of the tile, 16 bytes (block rows 2h, 2h + 1)
+      const int lr = t >> 1, h = t & 1;
+      if (lr < valid_cols) {
+        const uint2 a = tbuf[2 * h][lr], b = tbuf[2 * h + 1][lr];
+        *reinterpret_cast<uint4*>(owt.codes + (c0 + lr) * (rows >> 1) + (r0 >> 1) + 16 * h) =
+            make_uint4(a.x, a.y, b.x, b.y);
       }
     }
   }
