@@ -5,8 +5,10 @@
 // Method: "Pretraining Large Language Models with NVFP4" (gist.science
 // summary), Resumo técnico §2 Metodologia.  One layer step enqueues, on the
 // caller's stream:
-//   fwd: amax(X) and amax(Hadamard(X^T)) in one read; amax(W);
+//   fwd: amax(X) and amax(Hadamard(X^T)) in one read;
 //        X -> {X rowwise RNE, X^T Hadamard RNE} in one read;
+//        meanwhile, on the library's side stream of the device (forked from
+//        and joined back into the caller's stream with events): amax(W),
 //        W -> {W, W^T} with 16x16 blocks (item 3);
 //        Y = X W^T on the tensor cores.
 //   bwd: amax(dY) and amax(Hadamard(dY^T)) in one read;
@@ -16,6 +18,7 @@
 
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -244,6 +247,32 @@ void fill_views(uint8_t* ws, int64_t M, int64_t K, int64_t N, nvfp4_linear_views
   }
 }
 
+// Per-device side stream and fork/join events of nvfp4_linear_fwd, created
+// on first use.  The mutex is held while a call enqueues its fork, its side
+// work and its join, so calls from several host threads do not interleave
+// them (an event wait captures the event's state when it is enqueued).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mutex;
+SideStream g_side[64];
+
+cudaError_t side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
 nvfp4_status check_linear(int64_t M, int64_t K, int64_t N, void* ws, size_t ws_bytes) {
   if (!ws) return NVFP4_ERR_ARG;
   if (M <= 0 || K <= 0 || N <= 0 || M % 128 || K % 128 || N % 128) return NVFP4_ERR_SHAPE;
@@ -275,11 +304,24 @@ nvfp4_status nvfp4_linear_fwd(const void* x, const void* w, int64_t M, int64_t K
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   nvfp4_linear_views v;
   fill_views(static_cast<uint8_t*>(ws), M, K, N, &v);
-  cudaError_t e = launch_amax(x, M, K, v.xq.amax, nullptr, v.xtq.amax, seed, s);
-  if (e == cudaSuccess) e = launch_amax(w, N, K, v.wq.amax, nullptr, nullptr, 0, s);
+  // W's quantization (HBM-bound) overlaps X's (partly ALU-bound)
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  SideStream* ss = nullptr;
+  cudaError_t e = side_stream(&ss);
+  if (e == cudaSuccess) e = cudaEventRecord(ss->fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+  if (e == cudaSuccess) e = launch_amax(w, N, K, v.wq.amax, nullptr, nullptr, 0, ss->s);
+  if (e == cudaSuccess) e = launch_quant_2d(w, N, K, v.wq, &v.wtq, v.wq.amax, ss->s);
+  if (e == cudaSuccess) e = launch_amax(x, M, K, v.xq.amax, nullptr, v.xtq.amax, seed, s);
   if (e == cudaSuccess)
     e = launch_quant_tile(x, M, K, &v.xq, v.xq.amax, &v.xtq, v.xtq.amax, true, false, seed, 0, 0, s);
-  if (e == cudaSuccess) e = launch_quant_2d(w, N, K, v.wq, &v.wtq, v.wq.amax, s);
+  if (ss) {
+    // join even after an error above, so the caller's stream never runs
+    // ahead of side work that was enqueued
+    const cudaError_t ej = cudaEventRecord(ss->join, ss->s);
+    const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(s, ss->join, 0) : ej;
+    if (e == cudaSuccess) e = ew;
+  }
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
   return launch_gemm(v.xq, v.wq, y, NVFP4_OUT_BF16, N, s);
 }
