@@ -193,15 +193,35 @@ __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
   return philox4x32_10(u32x4{0u, 0u, kRhtStream, 0u}, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
 }
 
+// NaN-propagating max of m and |v| (a NaN anywhere makes the result NaN, so
+// it keeps the non-finite detection of a bit-pattern max).
+__device__ __forceinline__ float fmax_nan_abs(float m, float v) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(v)));
+  return r;
+}
+
+// Sign flips of Q on packed BF16 words of row (token) j: both halves of a
+// word belong to row j, so one XOR flips both.
+__device__ __forceinline__ uint32_t rht_sign_word(uint32_t sign_mask, int j) {
+  return ((sign_mask >> j) & 1u) * 0x80008000u;
+}
+
 // Q = 1/4 H16 diag(s) on 16 values in registers: sign flips (exact), the
 // in-place butterfly with strides 1, 2, 4, 8 (which sums the products
 // H[i][j] s_j x_j as a pairwise tree in index order), then * 0.25.  A zero
 // has no sign in Q x, so exact-zero outputs are made +0 (adding +0 does
 // that and leaves every other value unchanged); the butterfly and other
 // summation orders differ only in the sign of exact zeros.
+__device__ __forceinline__ void rht16_unsigned(float* v);
 __device__ __forceinline__ void rht16(float* v, uint32_t sign_mask) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((sign_mask >> j) & 1u) << 31));
+  rht16_unsigned(v);
+}
+
+// rht16 for values whose signs were already flipped (rht_sign_word).
+__device__ __forceinline__ void rht16_unsigned(float* v) {
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll

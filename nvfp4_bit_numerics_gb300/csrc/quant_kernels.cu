@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
   const uint32_t smask = rht_sign_mask(seed);
   const int64_t groups = cols >> 3;
   const int64_t units = (rows >> 4) * groups;
-  uint32_t mp = 0, mr = 0;
+  uint32_t mp2 = 0;  // max |x| of both BF16 halves, on the bit patterns
+  float mr = 0.0f;
   for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += (int64_t)gridDim.x * kThreads) {
     const int64_t rb = u / groups, cg = u - rb * groups;
     const uint16_t* p = x + (rb * 16) * cols + cg * 8;
@@ -115,21 +116,27 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
 #pragma unroll
     for (int i = 0; i < 16; ++i) q[i] = ldg_nc_v4(p + i * cols);
 #pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      mp2 = __vmaxu2(__vmaxu2(mp2, q[i].x & 0x7FFF7FFFu),
+                     __vmaxu2(__vmaxu2(q[i].y & 0x7FFF7FFFu, q[i].z & 0x7FFF7FFFu), q[i].w & 0x7FFF7FFFu));
+      const uint32_t sw = rht_sign_word(smask, i);  // row i of the chunk
+      q[i].x ^= sw; q[i].y ^= sw; q[i].z ^= sw; q[i].w ^= sw;
+    }
+#pragma unroll
     for (int c = 0; c < 8; ++c) {
       float v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint32_t w = (c < 2) ? q[i].x : (c < 4) ? q[i].y : (c < 6) ? q[i].z : q[i].w;
         v[i] = (c & 1) ? bf16hi(w) : bf16lo(w);
-        mp = max(mp, abs_bits(v[i]));
       }
-      rht16(v, smask);
+      rht16_unsigned(v);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) mr = max(mr, abs_bits(v[i]));
+      for (int i = 0; i < 16; ++i) mr = fmax_nan_abs(mr, v[i]);
     }
   }
-  if (out_plain) warp_amax_to_global(mp, out_plain, status);
-  warp_amax_to_global(mr, out_rht, status);
+  if (out_plain) warp_amax_to_global(max(mp2 & 0xFFFFu, mp2 >> 16) << 16, out_plain, status);
+  warp_amax_to_global(__float_as_uint(mr), out_rht, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -275,13 +282,14 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
       float va[16], vb[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(16 * ch + i) * kTilePitch + pc]);
+        uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(16 * ch + i) * kTilePitch + pc]);
+        if constexpr (kRHT) w ^= rht_sign_word(smask, i);  // both columns are in row i
         va[i] = bf16lo(w);
         vb[i] = bf16hi(w);
       }
       if constexpr (kRHT) {
-        rht16(va, smask);
-        rht16(vb, smask);
+        rht16_unsigned(va);
+        rht16_unsigned(vb);
       }
       const int64_t gm = m0 + 16 * ch;  // column of the transposed tensor
 #pragma unroll
@@ -363,15 +371,17 @@ __global__ void __launch_bounds__(kThreads, 3) quant_2d_kernel(const uint16_t* _
       unpack8(sp[0], v + 16 * h);
       unpack8(sp[1], v + 16 * h + 8);
     }
-    uint32_t m = 0;
+    // block amax as a float max of |v| (the tensor's amax pass reports
+    // non-finite input)
+    float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) m = max(m, abs_bits(v[i]));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
     uint32_t E;
     float enc;
-    block_scale(__uint_as_float(m), s_tensor, E, enc);
+    block_scale(m, s_tensor, E, enc);
     if (rp == 0) {
       s_E[br][bc] = E;
       s_enc[br][bc] = enc;
