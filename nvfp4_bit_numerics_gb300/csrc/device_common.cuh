@@ -155,7 +155,8 @@ struct u32x4 {
   uint32_t x, y, z, w;
 };
 
-__device__ __forceinline__ u32x4 philox4x32_10(u32x4 c, uint32_t k0, uint32_t k1) {
+// With the key schedule computed inline (for calls made once per thread).
+__device__ __forceinline__ u32x4 philox4x32_10_seed(u32x4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     if (r) {
@@ -168,15 +169,43 @@ __device__ __forceinline__ u32x4 philox4x32_10(u32x4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// The ten round keys of a 64-bit seed (round r uses lo32(seed) + r W0 and
+// hi32(seed) + r W1), computed on the host and passed as a __grid_constant__
+// kernel parameter, so that each key is a constant-bank operand of its XOR
+// instead of an add repeated in every call.
+struct PhiloxKey {
+  uint32_t k[20];
+};
+inline PhiloxKey philox_key(uint64_t seed) {
+  PhiloxKey key;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    key.k[2 * r] = k0;
+    key.k[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return key;
+}
+
+__device__ __forceinline__ u32x4 philox4x32_10(u32x4 c, const PhiloxKey& key) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u, p1 = (uint64_t)c.z * 0xCD9E8D57u;
+    c = u32x4{(uint32_t)(p1 >> 32) ^ c.y ^ key.k[2 * r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ key.k[2 * r + 1],
+              (uint32_t)p0};
+  }
+  return c;
+}
+
 // The stochastic-rounding inputs nu = 2^22 - 1 - 64 u of 16 consecutive
 // elements starting at e0 (e0 % 8 == 0): their uniforms u come from two
 // Philox calls with counters (e0/8, e0/8 + 1), low half of each word first.
-__device__ __forceinline__ void sr_nu16(uint64_t seed, uint32_t stream, uint64_t e0, uint32_t* nu) {
-  const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+__device__ __forceinline__ void sr_nu16(const PhiloxKey& key, uint32_t stream, uint64_t e0, uint32_t* nu) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint64_t g = (e0 >> 3) + h;
-    const u32x4 w = philox4x32_10(u32x4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, k0, k1);
+    const u32x4 w = philox4x32_10(u32x4{(uint32_t)g, (uint32_t)(g >> 32), stream, 0u}, key);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -190,7 +219,7 @@ __device__ __forceinline__ void sr_nu16(uint64_t seed, uint32_t stream, uint64_t
 // Philox(seed, (0, 0, 2, 0)), low 16 bits.
 constexpr uint32_t kRhtStream = 2;
 __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
-  return philox4x32_10(u32x4{0u, 0u, kRhtStream, 0u}, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
+  return philox4x32_10_seed(u32x4{0u, 0u, kRhtStream, 0u}, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
 }
 
 // NaN-propagating max of m and |v| (a NaN anywhere makes the result NaN, so
@@ -246,7 +275,7 @@ __device__ __forceinline__ void rht16_unsigned(float* v) {
 // enc_tab: the tensor's table of fill_enc_table.
 template <bool kSR>
 __device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, const float* enc_tab, uint32_t& E,
-                                            uint64_t seed, uint32_t stream, uint64_t e0) {
+                                            const PhiloxKey& key, uint32_t stream, uint64_t e0) {
   // block amax as a float max of |v| (the absolute value is an operand
   // modifier); equal to the bit-pattern max for finite values, and the
   // tensor's amax pass already reports non-finite input
@@ -260,7 +289,7 @@ __device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, const f
   for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(v[i], enc);
   if constexpr (kSR) {
     uint32_t nu[16];
-    sr_nu16(seed, stream, e0, nu);
+    sr_nu16(key, stream, e0, nu);
 #pragma unroll
     for (int i = 0; i < 16; ++i) s[i] = e2m1_sr_value(s[i], nu[i]);
   }

@@ -160,7 +160,8 @@ template <bool kSR, bool kRHT>
 __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                  int64_t cols, const float* amax, uint8_t* codes,
                                                                  uint8_t* scales, int layout, float* ts_out,
-                                                                 uint64_t seed, uint32_t stream, uint32_t* status) {
+                                                                 uint64_t seed, const __grid_constant__ PhiloxKey key,
+                                                                 uint32_t stream, uint32_t* status) {
   const float s_enc = tensor_prologue(amax, ts_out, status);
   __shared__ float enc_tab[128];
   fill_enc_table(enc_tab, s_enc, threadIdx.x);
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t*
       unpack8(q[2 * b + 1], v + 8);
       if constexpr (kRHT) rht16(v, smask);
       uint32_t E;
-      const uint2 o = quantize16<kSR>(v, s_enc, enc_tab, E, seed, stream, (uint64_t)(r * cols + c0 + 16 * b));
+      const uint2 o = quantize16<kSR>(v, s_enc, enc_tab, E, key, stream, (uint64_t)(r * cols + c0 + 16 * b));
       cw[2 * b] = o.x;
       cw[2 * b + 1] = o.y;
       sc |= E << (8 * b);
@@ -223,7 +224,8 @@ constexpr int kTilePitch = 72;  // uint16 per smem row: 144 B, conflict-free 16 
 template <bool kRow, bool kT, bool kRHT, bool kSR>
 __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                               int64_t cols, TileOut orow, TileOut ot,
-                                                              uint64_t seed, uint32_t* status) {
+                                                              uint64_t seed, const __grid_constant__ PhiloxKey key,
+                                                              uint32_t* status) {
   __shared__ __align__(16) uint16_t tile[kTileRows * kTilePitch];
   const int t = threadIdx.x;
   const int64_t tiles_c = cols / kTile;
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
         unpack8(sp[1], v + 8);
         uint32_t E;
         const uint2 o =
-            quantize16<kSR>(v, s_row, enc_tab[0], E, seed, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
+            quantize16<kSR>(v, s_row, enc_tab[0], E, key, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
         cw[2 * b] = o.x;
         cw[2 * b + 1] = o.y;
         sc |= E << (8 * b);
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
       for (int h = 0; h < 2; ++h) {
         const int64_t gr = c0 + pc + h;  // row of the transposed tensor
         uint32_t E;
-        const uint2 o = quantize16<kSR>(h ? vb : va, s_t, enc_tab[1], E, seed, ot.stream, (uint64_t)(gr * rows + gm));
+        const uint2 o = quantize16<kSR>(h ? vb : va, s_t, enc_tab[1], E, key, ot.stream, (uint64_t)(gr * rows + gm));
         *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = o;
         ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)E;
       }
@@ -489,9 +491,10 @@ cudaError_t launch_quant_rowwise(const void* x, int64_t rows, int64_t cols, cons
                                  cudaStream_t s) {
   const int64_t units = rows * (cols / 64);
   const int grid = grid_for(units, 8);
+  const PhiloxKey key = philox_key(seed);
   auto args = [&](auto kern) {
     kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), rows, cols, amax, out.codes, out.scales,
-                                   out.scale_layout, out.tensor_scale, seed, stream_id, device_status_ptr());
+                                   out.scale_layout, out.tensor_scale, seed, key, stream_id, device_status_ptr());
   };
   if (sr) {
     if (rht) args(quant_rowwise_kernel<true, true>);
@@ -517,7 +520,9 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
   uint32_t* status = device_status_ptr();
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   const bool row = out_row != nullptr, tr = out_t != nullptr;
-#define NVFP4_TILE(R, T, H, S) quant_tile_kernel<R, T, H, S><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot, seed, status)
+  const PhiloxKey key = philox_key(seed);
+#define NVFP4_TILE(R, T, H, S) \
+  quant_tile_kernel<R, T, H, S><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot, seed, key, status)
   if (row && tr) {
     if (rht_t) { if (sr) NVFP4_TILE(true, true, true, true); else NVFP4_TILE(true, true, true, false); }
     else       { if (sr) NVFP4_TILE(true, true, false, true); else NVFP4_TILE(true, true, false, false); }
