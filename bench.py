@@ -143,6 +143,42 @@ def traffic_record():
     return rec.get("dram_bytes_per_launch")
 
 
+def time_ms(fn, stream, reps=10, warm=2):
+    """Mean device time of fn() on `stream` (CUDA events)."""
+    import torch
+
+    for _ in range(warm):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def library_gemms(pairs, stream):
+    """For context only (never the product path): the same GEMMs through
+    cuBLAS BF16 (torch.matmul) and cuBLASLt's NVFP4 GEMM (torch._scaled_mm on
+    this library's own quantized operands, whose scale layout it accepts).
+    pairs: {name: (a_bf16, b_bf16, out_bf16, a_q, b_q)} with out = a @ b^T."""
+    import torch
+
+    res = {"cublas_bf16_ms": {}, "cublaslt_nvfp4_ms": {}}
+    for name, (a, b, out, qa, qb) in pairs.items():
+        res["cublas_bf16_ms"][name] = time_ms(lambda: torch.matmul(a, b.t(), out=out), stream)
+        try:
+            fa, fb = qa.codes.view(torch.float4_e2m1fn_x2), qb.codes.view(torch.float4_e2m1fn_x2)
+            sa, sb = qa.scales.view(torch.float8_e4m3fn), qb.scales.view(torch.float8_e4m3fn)
+            res["cublaslt_nvfp4_ms"][name] = time_ms(
+                lambda: torch._scaled_mm(fa, fb.t(), sa, sb, out_dtype=torch.bfloat16), stream)
+        except Exception as e:  # an older torch without FP4 types
+            res["cublaslt_nvfp4_ms"][name] = None
+            res["cublaslt_nvfp4_error"] = type(e).__name__
+    return res
+
+
 def cpu_oracle_step(x_f, w_f, dy_f):
     """One bounded oracle sample: the whole layer step for a 64-token slice of
     X and dY (all of W).  Returns (seconds, flops)."""
@@ -342,6 +378,16 @@ def run_gpu(args, rank, world, local):
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
     h2d = sum(t.numel() * t.element_size() for t in (x_h, w_h, dy_h))
 
+    # library GEMMs of the same three shapes, for context (after the timed
+    # regions; the quantized operands are the last step's workspace)
+    dyt, xt = dy.t().contiguous(), x.t().contiguous()
+    context = library_gemms({
+        "fprop": (x, w, y, v["xq"], v["wq"]),
+        "dgrad": (dy, w.t().contiguous(), dx, v["dyq"], v["wtq"]),
+        "wgrad": (dyt, xt, dw, v["dytq"], v["xtq"]),
+    }, stream)
+    del dyt, xt
+
     if rank != 0:
         return 0
     hbm, bf16, src = measured_peaks()
@@ -378,6 +424,8 @@ def run_gpu(args, rank, world, local):
                 "api": "nvfp4_linear_fwd + nvfp4_linear_bwd",
                 "overlap": "uploads of step i+1 and downloads of step i-1 overlap step i's kernels"},
         "gpu_launches": int(launches),
+        "context": dict(context, note="library GEMMs of the same shapes for comparison; not this "
+                                      "library's path (out = A B^T: Fprop X W^T, Dgrad dY W, Wgrad dY^T X)"),
         "clocks": clk,
         "cpu_baseline": {"value": cpu_flops / cpu_s / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle",
@@ -388,18 +436,77 @@ def run_gpu(args, rank, world, local):
     return 0
 
 
+def run_sweep(args, rank, world, local):
+    """--sweep: one JSON line per further configured shape (the layer step
+    for the MLP down-projection and the QKV projection; the GEMM alone for
+    the M = 16384 shape sweep), with the library GEMMs for context."""
+    import torch
+
+    from nvfp4_bit_numerics_gb300 import binding as B, build as nbuild, workloads
+
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    nbuild.build()
+    B.load_library()
+    stream = torch.cuda.current_stream(dev)
+    fp4_peak = measured_peaks()[1] * FP4_OVER_BF16
+    for name, gen, (m, k, n) in [("mlp_down", workloads.mlp_down, (8192, 20480, 5120)),
+                                 ("qkv", workloads.qkv, (8192, 5120, 7168))]:
+        x, w, dy = (t.to(dev) for t in gen())
+        ws = B.linear_workspace(m, k, n, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+
+        def api():
+            B.nvfp4_linear_fwd(x, w, SEED, ws, y=y, stream=stream)
+            B.nvfp4_linear_bwd(dy, k, SEED, ws, dx=dx, dw=dw, stream=stream)
+
+        ms = time_ms(api, stream, reps=args.steps, warm=args.warmup)
+        if B.nvfp4_get_status() != B.NVFP4_OK:
+            raise RuntimeError("device status in the sweep")
+        print(json.dumps({"sweep": "layer", "workload": "%s_%dx%dx%d" % (name, m, k, n), "ms_per_step": ms,
+                          "value": 6.0 * m * k * n / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "pct_fp4_peak": 100.0 * 6.0 * m * k * n / (ms * 1e-3) / 1e12 / fp4_peak}), flush=True)
+        del x, w, dy, ws, y, dx, dw
+    for (k, n) in [(4096, 4096), (5120, 5120), (8192, 8192), (5120, 20480), (20480, 5120)]:
+        m = 16384
+        x, w, _ = (t.to(dev) for t in workloads.gemm_sweep(k, n))
+        qa = B.empty_qtensor(m, k, device=dev)
+        qb = B.empty_qtensor(n, k, device=dev)
+        B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE, B.NVFP4_ROUND_RNE, out=qa)
+        B.nvfp4_quantize(w, B.NVFP4_Q_2D, out=qb)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ms = time_ms(lambda: B.nvfp4_gemm(qa, qb, out=y), stream, reps=args.steps, warm=args.warmup)
+        if B.nvfp4_get_status() != B.NVFP4_OK:
+            raise RuntimeError("device status in the sweep")
+        tf = 2.0 * m * k * n / (ms * 1e-3) / 1e12
+        ctx = library_gemms({"gemm": (x, w, y, qa, qb)}, stream)
+        print(json.dumps({"sweep": "gemm", "workload": "gemm_%dx%dx%d" % (m, k, n), "ms": ms, "value": tf,
+                          "unit": "TFLOP/s", "pct_fp4_peak": 100.0 * tf / fp4_peak,
+                          "cublas_bf16_ms": ctx["cublas_bf16_ms"]["gemm"],
+                          "cublaslt_nvfp4_ms": ctx["cublaslt_nvfp4_ms"]["gemm"]}), flush=True)
+        del x, w, qa, qb, y
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark line, one line per further configured shape")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gpu":
         args.warmup = 3
     rank, world, local = dist_info()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.sweep:
+        return run_sweep(args, rank, world, local)
     return run_gpu(args, rank, world, local)
 
 
