@@ -212,6 +212,14 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d_de
  *            writes the saved operands there and bwd reads them, so the same
  *            workspace must be passed to both, untouched in between.
  * Sizes: M, K, N positive multiples of 128.
+ * Streams: everything is ordered on `stream`.  Outside stream capture, fwd
+ * runs W's amax and 2D quantization on a side stream that the library
+ * creates once per device, forked from `stream` and joined back into it with
+ * events before the GEMM (so it overlaps X's quantization); calls from several
+ * host threads are serialised while they enqueue.  While `stream` is being
+ * captured into a graph, fwd enqueues all of its work on `stream` itself.
+ * Make the first call on a device outside capture (it creates the side
+ * stream and sets kernel attributes).
  */
 size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t K, int64_t N);
 nvfp4_status nvfp4_linear_fwd(const void* x_dev, const void* w_dev, int64_t M, int64_t K, int64_t N,

@@ -8,7 +8,8 @@
 //   fwd: amax(X) and amax(Hadamard(X^T)) in one read;
 //        X -> {X rowwise RNE, X^T Hadamard RNE} in one read;
 //        meanwhile, on the library's side stream of the device (forked from
-//        and joined back into the caller's stream with events): amax(W),
+//        and joined back into the caller's stream with events; on the
+//        caller's stream itself while it is being captured): amax(W),
 //        W -> {W, W^T} with 16x16 blocks (item 3);
 //        Y = X W^T on the tensor cores.
 //   bwd: amax(dY) and amax(Hadamard(dY^T)) in one read;
@@ -304,14 +305,28 @@ nvfp4_status nvfp4_linear_fwd(const void* x, const void* w, int64_t M, int64_t K
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   nvfp4_linear_views v;
   fill_views(static_cast<uint8_t*>(ws), M, K, N, &v);
-  // W's quantization (HBM-bound) overlaps X's (partly ALU-bound)
-  std::lock_guard<std::mutex> lock(g_side_mutex);
+  // W's quantization (HBM-bound) overlaps X's (partly ALU-bound).  Under
+  // stream capture nothing is forked: a stream that joins a capture stays in
+  // it until the capture ends, and the side stream is shared by every caller
+  // on the device, so all of the layer is enqueued on the caller's stream.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    cap = cudaStreamCaptureStatusActive;
+  }
+  const bool fork = cap == cudaStreamCaptureStatusNone;
+  std::unique_lock<std::mutex> lock(g_side_mutex, std::defer_lock);
   SideStream* ss = nullptr;
-  cudaError_t e = side_stream(&ss);
-  if (e == cudaSuccess) e = cudaEventRecord(ss->fork, s);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
-  if (e == cudaSuccess) e = launch_amax(w, N, K, v.wq.amax, nullptr, nullptr, 0, ss->s);
-  if (e == cudaSuccess) e = launch_quant_2d(w, N, K, v.wq, &v.wtq, v.wq.amax, ss->s);
+  cudaError_t e = cudaSuccess;
+  if (fork) {
+    lock.lock();
+    e = side_stream(&ss);
+    if (e == cudaSuccess) e = cudaEventRecord(ss->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+  }
+  cudaStream_t sw = fork ? (ss ? ss->s : s) : s;
+  if (e == cudaSuccess) e = launch_amax(w, N, K, v.wq.amax, nullptr, nullptr, 0, sw);
+  if (e == cudaSuccess) e = launch_quant_2d(w, N, K, v.wq, &v.wtq, v.wq.amax, sw);
   if (e == cudaSuccess) e = launch_amax(x, M, K, v.xq.amax, nullptr, v.xtq.amax, seed, s);
   if (e == cudaSuccess)
     e = launch_quant_tile(x, M, K, &v.xq, v.xq.amax, &v.xtq, v.xtq.amax, true, false, seed, 0, 0, s);

@@ -1,0 +1,110 @@
+"""The layer step under CUDA graph capture and from concurrent host threads.
+
+Outside capture, nvfp4_linear_fwd quantizes W on the library's per-device
+side stream (forked from and joined back into the caller's stream); under
+capture it enqueues everything on the caller's stream.  Both paths, and two
+host threads driving their own layers at once, must give exactly the results
+of a plain single-threaded run."""
+
+import threading
+
+import pytest
+import torch
+
+from nvfp4_bit_numerics_gb300 import binding as B
+from nvfp4_bit_numerics_gb300 import workloads
+from tests.gpu_util import ensure_lib
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = (512, 768, 1024)  # M, K, N: multiples of 256, the CTA-pair GEMM
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    return ensure_lib()
+
+
+def inputs(seed):
+    M, K, N = SHAPE
+    x, w, dy = workloads.layer_inputs(M, K, N, seed, 4, 30.0, 0.02, 1e-3)
+    return x.cuda(), w.cuda(), dy.cuda()
+
+
+def eager(x, w, dy, seed):
+    M, K = x.shape
+    N = w.shape[0]
+    ws = B.linear_workspace(M, K, N)
+    y = B.nvfp4_linear_fwd(x, w, seed, ws)
+    dx, dw = B.nvfp4_linear_bwd(dy, K, seed, ws)
+    torch.cuda.synchronize()
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    return y, dx, dw
+
+
+def test_graph_capture_replays_bit_identical():
+    M, K, N = SHAPE
+    x, w, dy = inputs(11)
+    seed = 77
+    ref = eager(x, w, dy, seed)
+    ws = B.linear_workspace(M, K, N)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.nvfp4_linear_fwd(x, w, seed, ws, y=y, stream=s)
+        B.nvfp4_linear_bwd(dy, K, seed, ws, dx=dx, dw=dw, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.nvfp4_linear_fwd(x, w, seed, ws, y=y, stream=s)
+        B.nvfp4_linear_bwd(dy, K, seed, ws, dx=dx, dw=dw, stream=s)
+    for _ in range(3):
+        for t in (y, dx, dw):
+            t.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for got, want in zip((y, dx, dw), ref):
+            assert torch.equal(got, want)
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+
+
+def test_concurrent_host_threads():
+    """Two threads, each with its own stream, workspace and layer, enqueue
+    twenty steps at the same time; the shared side stream must keep them
+    apart."""
+    M, K, N = SHAPE
+    seeds = [5, 6]
+    data = [inputs(100 + i) for i in range(2)]
+    refs = [eager(*data[i], seeds[i]) for i in range(2)]
+    results = [None, None]
+    errors = []
+    start = threading.Barrier(2)
+
+    def worker(i):
+        try:
+            x, w, dy = data[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                ws = B.linear_workspace(M, K, N)
+                start.wait()
+                for _ in range(20):
+                    y = B.nvfp4_linear_fwd(x, w, seeds[i], ws, stream=s)
+                    dx, dw = B.nvfp4_linear_bwd(dy, K, seeds[i], ws, stream=s)
+                s.synchronize()
+            results[i] = (y, dx, dw)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    for i in range(2):
+        for got, want in zip(results[i], refs[i]):
+            assert torch.equal(got, want), i
