@@ -20,6 +20,10 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kThreads = 256;
+// The kernels index their work units (tiles, 16-row chunks, 64-element row
+// groups) with 32-bit integers; the launchers refuse tensors with 2^31 units
+// or more (over 2^42 elements).
+constexpr int64_t kMaxUnits = int64_t(1) << 31;
 
 int sm_count() {
   static int cached[64] = {0};
@@ -106,11 +110,13 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
                                                                  uint32_t* out_rht, uint32_t* status) {
   const uint32_t smask = rht_sign_mask(seed);
   const int64_t groups = cols >> 3;
-  const int64_t units = (rows >> 4) * groups;
+  // unit counts are below 2^32 (the launcher checks), so the index math is
+  // 32-bit: a 64-bit division is a long subroutine
+  const uint32_t units = (uint32_t)((rows >> 4) * groups), groups32 = (uint32_t)groups;
   uint32_t mp2 = 0;  // max |x| of both BF16 halves, on the bit patterns
   float mr = 0.0f;
-  for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += (int64_t)gridDim.x * kThreads) {
-    const int64_t rb = u / groups, cg = u - rb * groups;
+  for (uint32_t u = blockIdx.x * kThreads + threadIdx.x; u < units; u += gridDim.x * kThreads) {
+    const uint32_t rb = u / groups32, cg = u - rb * groups32;
     const uint16_t* p = x + (rb * 16) * cols + cg * 8;
     uint4 q[16];
 #pragma unroll
@@ -168,10 +174,10 @@ __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t*
   __syncthreads();
   const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
   const int64_t gpr = cols >> 6;  // 64-element groups per row
-  const int64_t units = rows * gpr;
+  const uint32_t units = (uint32_t)(rows * gpr), gpr32 = (uint32_t)gpr;  // < 2^32 (launcher)
   const int64_t n_kb = cols >> 4;
-  for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += (int64_t)gridDim.x * kThreads) {
-    const int64_t r = u / gpr, g = u - r * gpr;
+  for (uint32_t u = blockIdx.x * kThreads + threadIdx.x; u < units; u += gridDim.x * kThreads) {
+    const int64_t r = u / gpr32, g = u - (uint32_t)r * gpr32;
     const int64_t c0 = g * 64;
     const uint16_t* p = x + r * cols + c0;
     uint4 q[8];
@@ -241,9 +247,10 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
   if constexpr (kT) fill_enc_table(enc_tab[1], s_t, t - 128);
   const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
 
-  for (int64_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
-    const int64_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
-    const int64_t m0 = tm * kTileRows, c0 = tc * kTile;
+  const uint32_t tiles_c32 = (uint32_t)tiles_c;  // tile counts < 2^32 (launcher): 32-bit index math
+  for (uint32_t tl = blockIdx.x; tl < (uint32_t)n_tiles; tl += gridDim.x) {
+    const uint32_t tm = tl / tiles_c32, tc = tl - tm * tiles_c32;
+    const int64_t m0 = (int64_t)tm * kTileRows, c0 = (int64_t)tc * kTile;
     const int valid = rows - m0 < kTileRows ? (int)(rows - m0) : kTileRows;  // 64 or 128
     uint4 q[4];
 #pragma unroll
@@ -339,9 +346,10 @@ __global__ void __launch_bounds__(kThreads, 3) quant_2d_kernel(const uint16_t* _
 
   // the next tile's loads are issued before the current tile is processed
   uint4 q[4];
-  auto load_tile = [&](int64_t tl) {
-    const int64_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
-    const int64_t r0 = tm * k2dRows, c0 = tc * k2dCols;
+  const uint32_t tiles_c32 = (uint32_t)tiles_c;  // tile counts < 2^32 (launcher): 32-bit index math
+  auto load_tile = [&](uint32_t tl) {
+    const uint32_t tm = tl / tiles_c32, tc = tl - tm * tiles_c32;
+    const int64_t r0 = (int64_t)tm * k2dRows, c0 = (int64_t)tc * k2dCols;
     const int valid_cols = cols - c0 < k2dCols ? (int)(cols - c0) : k2dCols;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -351,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 3) quant_2d_kernel(const uint16_t* _
     }
   };
   if (blockIdx.x < n_tiles) load_tile(blockIdx.x);
-  for (int64_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
-    const int64_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
-    const int64_t r0 = tm * k2dRows, c0 = tc * k2dCols;
+  for (uint32_t tl = blockIdx.x; tl < (uint32_t)n_tiles; tl += gridDim.x) {
+    const uint32_t tm = tl / tiles_c32, tc = tl - tm * tiles_c32;
+    const int64_t r0 = (int64_t)tm * k2dRows, c0 = (int64_t)tc * k2dCols;
     const int valid_cols = cols - c0 < k2dCols ? (int)(cols - c0) : k2dCols;  // 64 or 128
     __syncthreads();  // the previous tile's readers are done
 #pragma unroll
@@ -462,6 +470,7 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, float* plain,
   }
   const int64_t n = rows * cols;
   if (n == 0) return cudaSuccess;
+  if ((rows / 16) * (cols / 8) >= kMaxUnits) return cudaErrorInvalidValue;
   // the plain amax rides along with the first transform pass that runs
   if (o_cols) {
     const int64_t units = (rows / 16) * (cols / 8);
@@ -490,6 +499,7 @@ cudaError_t launch_quant_rowwise(const void* x, int64_t rows, int64_t cols, cons
                                  const float* amax, bool rht, bool sr, uint64_t seed, uint32_t stream_id,
                                  cudaStream_t s) {
   const int64_t units = rows * (cols / 64);
+  if (units >= kMaxUnits) return cudaErrorInvalidValue;
   const int grid = grid_for(units, 8);
   const PhiloxKey key = philox_key(seed);
   auto args = [&](auto kern) {
@@ -515,6 +525,7 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
                               stream_row};
   if (out_t) ot = TileOut{out_t->codes, out_t->scales, amax_t, out_t->tensor_scale, out_t->scale_layout, stream_t};
   const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * (cols / kTile);
+  if (tiles >= kMaxUnits) return cudaErrorInvalidValue;
   const int64_t cap = (int64_t)sm_count() * 8;
   const dim3 grid((unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap));
   uint32_t* status = device_status_ptr();
@@ -543,6 +554,7 @@ cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvf
   TileOut owt{};
   if (out_t) owt = TileOut{out_t->codes, out_t->scales, amax, out_t->tensor_scale, out_t->scale_layout, 0};
   const int64_t tiles = (rows / k2dRows) * ((cols + k2dCols - 1) / k2dCols);
+  if (tiles >= kMaxUnits) return cudaErrorInvalidValue;
   const int64_t cap = (int64_t)sm_count() * 8;
   const unsigned grid = (unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
   quant_2d_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(w), rows, cols, amax, ow, owt,
