@@ -7,7 +7,10 @@
 // take NVFP4 natively) -- Fprop, Dgrad and Wgrad of a linear layer, each a
 // product of two K-major NVFP4 operands with FP32 accumulation.
 //
-// Design (one CTA per SM, persistent over 128 x BN output tiles):
+// Two kernels.  For M and N multiples of 256, nvfp4_gemm_pair_kernel (CTA
+// pairs, 256 x 256 tiles, tcgen05.mma.cta_group::2; described before it
+// below).  Otherwise the single-CTA kernel, whose design is:
+// (one CTA per SM, persistent over 128 x BN output tiles)
 //   warp 0      TMA producer: 2D tiled loads of the packed codes (128-byte
 //               rows, 128B swizzle) and 1D bulk loads of the scale tiles,
 //               into a ring of shared-memory stages guarded by mbarriers.
@@ -493,9 +496,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //   warp 0      producer (both CTAs): waits its own `empty` barrier, loads
 //               its A and B halves; the copies signal the even CTA's `full`
 //               barrier, which the even CTA's producer armed for both.
-//   warp 14     scale producer (both CTAs): fills a ring of 8 shared-memory
-//               scale slots ahead of the MMAs, so scale loads are off the
-//               stage-to-stage critical path.
+//   warp 14     scale producer (both CTAs): fills a ring of 4 shared-memory
+//               scale slots ahead of the staging warps, so scale loads are
+//               off the stage-to-stage critical path.
 //   warp 1      even CTA: MMA issuer with one barrier wait per stage
 //               (`sf_ready`, which the even CTA's staging warps arrive on only
 //               after `full`); commits multicast to both CTAs.
@@ -507,11 +510,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //               CTA's `sf_ready` barrier of the region.  The three rings
 //               (6 operand stages, 4 scale slots, 5 scale regions) are
 //               decoupled so the operand ring is as deep as shared memory
-//               allows.  A scale load is issued when its slot is freed by
-//               the staging of the stage 4 earlier and lands ~1 us later, so
-//               the slot count bounds the staging rate at about
-//               (load latency + staging time) / slots per stage: with 3
-//               slots that, not the tensor pipe, set the main-loop pace.
+//               allows.  A scale load is issued once the staging of the
+//               stage 4 earlier has freed its slot, and lands about 1 us
+//               later (a fourth slot, over three, was up to 3 % faster).
 //   warps 6-13  epilogue (both CTAs) for the CTA's 128 rows; they release
 //               the accumulator with a remote arrive on the even CTA, then
 //               write BF16 output as 32-row x 16-column boxes staged in a
