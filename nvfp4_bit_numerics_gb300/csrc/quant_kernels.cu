@@ -1,5 +1,5 @@
-// quant_kernels.cu -- bandwidth-bound NVFP4 kernels for sm_103a: global
-// amax, 1x16 rowwise quantization, the 64x64 tile kernel that writes the
+// quant_kernels.cu -- the NVFP4 quantization kernels for sm_103a: global
+// amax, 1x16 rowwise quantization, the 128x64 tile kernel that writes the
 // rowwise and/or the transposed (token-major, Hadamard-transformed) operand
 // from one read, and the 16x16 2D weight quantization that writes W and W^T.
 //
@@ -10,7 +10,10 @@
 //
 // All kernels read BF16 with 16-byte vector loads, keep their working set in
 // registers or a small shared-memory tile, and write packed codes with 8- or
-// 16-byte stores; they are bound by HBM bandwidth.
+// 16-byte stores.  The plain amax and the RNE passes are bound by HBM
+// bandwidth; the passes that transform (Hadamard) or round stochastically
+// (Philox and the rounding itself per element) are bound by instruction
+// throughput, which is what their arithmetic is arranged to minimise.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
