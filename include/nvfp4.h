@@ -196,6 +196,21 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d_de
                         int64_t ldd, nvfp4_stream stream);
 
 /*
+ * nvfp4_gemm_amax -- nvfp4_gemm that also yields the amax its output's
+ * consumer needs: the global amax that sets the per-tensor scale of the next
+ * quantization (Resumo técnico §2, two-level scaling), taken in the epilogue
+ * instead of by a separate read of D.
+ *   amax_dev  one float in device memory, 4-byte aligned; zeroed on `stream`
+ *             first, then it receives max |D| over the stored values (after
+ *             BF16 rounding for BF16 output; +inf or NaN if D holds one).
+ *             Pass it to nvfp4_quantize of D with compute_amax = 0 as the
+ *             output tensor's amax.
+ * Other arguments, sizes and errors as nvfp4_gemm.
+ */
+nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d_dev, int32_t d_dtype,
+                             int64_t ldd, float* amax_dev, nvfp4_stream stream);
+
+/*
  * One NVFP4 linear layer Y = X W^T, X [M, K] tokens x in-features, W [N, K].
  *
  * nvfp4_linear_fwd: amax of X, of the Hadamard-transformed X^T and of W;

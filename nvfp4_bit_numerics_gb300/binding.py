@@ -43,7 +43,7 @@ EXPORTED = [
     "nvfp4_amax", "nvfp4_quantize", "nvfp4_scale_bytes", "nvfp4_gemm", "nvfp4_linear_workspace_bytes",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_linear_get_views", "nvfp4_get_status",
     "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
-    "nvfp4_debug_stall_next_gemm",
+    "nvfp4_debug_stall_next_gemm", "nvfp4_gemm_amax",
 ]
 
 
@@ -87,6 +87,7 @@ def load_library(path=LIB_PATH):
         "nvfp4_quantize": (I32, [P, I64, I64, ctypes.POINTER(nvfp4_quant_cfg), T, T, P]),
         "nvfp4_scale_bytes": (SZ, [I64, I64, I32]),
         "nvfp4_gemm": (I32, [T, T, P, I32, I64, P]),
+        "nvfp4_gemm_amax": (I32, [T, T, P, I32, I64, P, P]),
         "nvfp4_linear_workspace_bytes": (SZ, [I64, I64, I64]),
         "nvfp4_linear_fwd": (I32, [P, P, I64, I64, I64, U64, P, P, SZ, P]),
         "nvfp4_linear_bwd": (I32, [P, I64, I64, I64, U64, P, P, P, SZ, P]),
@@ -190,6 +191,20 @@ def nvfp4_gemm(a, b, out=None, out_dtype=torch.bfloat16, stream=None):
     _check("nvfp4_gemm", load_library().nvfp4_gemm(ctypes.byref(sa), ctypes.byref(sb), _ptr(out), dt,
                                                    out.stride(0), _stream(stream)))
     return out
+
+
+def nvfp4_gemm_amax(a, b, out=None, out_dtype=torch.bfloat16, amax=None, stream=None):
+    """nvfp4_gemm that also returns max |D| over the stored output (a float32
+    device tensor of one element): (out, amax)."""
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=out_dtype, device=a.codes.device)
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=a.codes.device)
+    dt = NVFP4_OUT_F32 if out.dtype == torch.float32 else NVFP4_OUT_BF16
+    sa, sb = a.struct(), b.struct()
+    _check("nvfp4_gemm_amax", load_library().nvfp4_gemm_amax(ctypes.byref(sa), ctypes.byref(sb), _ptr(out), dt,
+                                                             out.stride(0), _ptr(amax), _stream(stream)))
+    return out, amax
 
 
 def nvfp4_linear_workspace_bytes(M, K, N):

@@ -199,6 +199,25 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, i
   return launch_gemm(*a, *b, d, d_dtype, ldd, static_cast<cudaStream_t>(stream));
 }
 
+nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int32_t d_dtype, int64_t ldd,
+                             float* amax_dev, nvfp4_stream stream) {
+  if (!amax_dev) return NVFP4_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(amax_dev) & 3u) != 0) return NVFP4_ERR_ALIGN;
+  // the same checks as nvfp4_gemm, on a call that launches nothing
+  if (!valid_tensor(a) || !valid_tensor(b) || !d) return NVFP4_ERR_ARG;
+  if (d_dtype != NVFP4_OUT_BF16 && d_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
+  if (a->scale_layout != NVFP4_SCALES_MMA || b->scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_ARG;
+  const int64_t M = a->rows, N = b->rows, K = a->cols;
+  if (M <= 0 || N <= 0 || K <= 0 || b->cols != K) return NVFP4_ERR_SHAPE;
+  if (M % 128 || N % 128 || K % 64 || ldd < N) return NVFP4_ERR_SHAPE;
+  if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return NVFP4_ERR_SHAPE;
+  const int64_t esz = d_dtype == NVFP4_OUT_F32 ? 4 : 2;
+  if (!aligned16(d) || (ldd * esz) % 16) return NVFP4_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(amax_dev, 0, sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return launch_gemm(*a, *b, d, d_dtype, ldd, s, amax_dev);
+}
+
 // ---------------------------------------------------------------------------
 // Linear layer
 // ---------------------------------------------------------------------------

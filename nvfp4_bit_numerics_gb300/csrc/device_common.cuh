@@ -65,11 +65,15 @@ __device__ __forceinline__ float tensor_encode_scale(float amax) {
 }
 __device__ __forceinline__ float tensor_decode_scale(float s_enc) { return __fdiv_rn(1.0f, s_enc); }
 
-// fl(a / 6) for a >= 0.  From 2^-120 up, q = fl(a * fl(1/6)) corrected by
-// one FMA on the exact remainder a - 6q is the correctly rounded quotient
-// (checked against a double-precision division for every float in
-// [2^-120, inf)); below, where a / 6 nears the subnormal range, the IEEE
-// division itself.
+// fl(a / 6) for a >= 0.  From 2^-120 up: q = fl(a * fl(1/6)), then one
+// correction with the exact remainder r = fma(-q, 6, a) and q' = fma(r,
+// fl(1/6), q) -- the remainder-correction step of FMA-based division
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990) applied to the
+// constant divisor 6.  q' equals the correctly rounded quotient for every
+// float in [2^-120, inf) (checked exhaustively against a double-precision
+// division); below, where a / 6 nears the subnormal range, the IEEE division
+// itself.
 __device__ __forceinline__ float div6_rn(float a) {
   if (a < 0x1p-120f) return __fdiv_rn(a, 6.0f);
   const float r6 = 1.0f / 6.0f;

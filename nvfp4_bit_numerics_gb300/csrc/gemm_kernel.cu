@@ -89,6 +89,7 @@ struct Params {
   int n_fastest;   // tile order: 1 = consecutive tiles walk N (B stays in L2)
   int debug_stall; // failure-detection test: the first stage's loads are never issued
   int tma_store;   // pair kernel: BF16 output written by bulk tensor stores
+  uint32_t* amax_out;  // if set: max |D| over the stored output, as float bits (atomicMax)
   uint32_t* status;
 };
 
@@ -226,6 +227,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// Output amax for the consumer of D (the next layer's quantization): the
+// largest |value| as stored.  BF16: max over the magnitude bit patterns of
+// packed pairs; FP32: max over the magnitude bits (NaN, whose bits exceed
+// inf's, propagates).  One atomic per warp; non-negative float bits order
+// like the floats.
+template <int kWords>
+__device__ __forceinline__ void amax_bf16_words(const uint32_t* packed, uint32_t* amax_out) {
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) m2 = __vmaxu2(m2, packed[i] & 0x7FFF7FFFu);
+  const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max(m2 & 0xFFFFu, m2 >> 16) << 16);
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(amax_out, m);
+}
+__device__ __forceinline__ void amax_bits_to_global(uint32_t m, uint32_t* amax_out) {
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(amax_out, m);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -443,6 +462,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int64_t row = (int64_t)mb * kBM + 32 * q + lane;
       const int64_t col0 = (int64_t)nb * BN + half * C::kEpiCols;
       uint32_t packed[C::kEpiCols / 2];
+      uint32_t m32 = 0;  // FP32 output: max magnitude bits
 #pragma unroll
       for (int c = 0; c < C::kEpiCols / 32; ++c) {
         uint32_t v[32];
@@ -456,11 +476,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         } else {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0 + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
-                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
-                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
-                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+          for (int i = 0; i < 8; ++i) {
+            const uint4 o = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
+                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
+                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
+                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+            dst[i] = o;
+            m32 = max(m32, max(max(o.x & 0x7FFFFFFFu, o.y & 0x7FFFFFFFu), max(o.z & 0x7FFFFFFFu, o.w & 0x7FFFFFFFu)));
+          }
         }
       }
       tc_fence_before();
@@ -472,6 +495,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::kEpiCols / 8; ++c)
           dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        if (p.amax_out) amax_bf16_words<C::kEpiCols / 2>(packed, p.amax_out);
+      } else if (p.amax_out) {
+        amax_bits_to_global(m32, p.amax_out);
       }
     }
   }
@@ -833,6 +859,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const int64_t row = (int64_t)mb * 256 + (int64_t)rank * 128 + 32 * q + lane;
       const int64_t col0 = (int64_t)nb * kPairBN + half * kCols;
       uint32_t packed[kCols / 2];
+      uint32_t m32 = 0;  // FP32 output: max magnitude bits
 #pragma unroll
       for (int c = 0; c < kCols / 32; ++c) {
         uint32_t v[32];
@@ -846,11 +873,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         } else {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0 + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
-                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
-                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
-                                __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+          for (int i = 0; i < 8; ++i) {
+            const uint4 o = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
+                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
+                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
+                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+            dst[i] = o;
+            m32 = max(m32, max(max(o.x & 0x7FFFFFFFu, o.y & 0x7FFFFFFFu), max(o.z & 0x7FFFFFFFu, o.w & 0x7FFFFFFFu)));
+          }
         }
       }
       tc_fence_before();
@@ -879,6 +909,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           __syncwarp();
           if (lane == 0) tma_store_2d(&tmap_d, (int)col0 + 16 * j, (int)(row - lane), buf);
         }
+        if (p.amax_out) amax_bf16_words<kCols / 2>(packed, p.amax_out);
+      } else if (p.amax_out) {
+        amax_bits_to_global(m32, p.amax_out);
       }
     }
     // the output is in global memory (and the buffers free) before exit
@@ -958,7 +991,7 @@ int sm_count() {
 
 template <int BN>
 nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                 cudaStream_t s) {
+                 float* amax_out, cudaStream_t s) {
   using C = Cfg<BN>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -989,6 +1022,7 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
   p.n_fastest = p.N < p.M;
   p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
+  p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
   p.tma_store = 0;
   const int tiles = (p.M / kBM) * (p.N / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
@@ -999,7 +1033,7 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
 
 
 nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                      cudaStream_t s) {
+                      float* amax_out, cudaStream_t s) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1029,6 +1063,7 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   p.n_fastest = p.N < p.M;
   p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
+  p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
   // BF16 output goes through bulk tensor stores (the API guarantees the
   // 16-byte aligned base and row stride they need); FP32 through plain stores
   CUtensorMap md = ma;  // unused for FP32 output
@@ -1047,10 +1082,10 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
 void set_gemm_debug_stall(int on) { g_debug_stall.store(on ? 1 : 0); }
 
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                         cudaStream_t s) {
-  if (a.rows % 256 == 0 && b.rows % 256 == 0) return run_pair(a, b, d, d_dtype, ldd, s);
-  if (b.rows % 256 == 0) return run<256>(a, b, d, d_dtype, ldd, s);
-  return run<128>(a, b, d, d_dtype, ldd, s);
+                         cudaStream_t s, float* amax_out) {
+  if (a.rows % 256 == 0 && b.rows % 256 == 0) return run_pair(a, b, d, d_dtype, ldd, amax_out, s);
+  if (b.rows % 256 == 0) return run<256>(a, b, d, d_dtype, ldd, amax_out, s);
+  return run<128>(a, b, d, d_dtype, ldd, amax_out, s);
 }
 
 }  // namespace nvfp4

@@ -45,8 +45,10 @@ cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvf
 // stage's loads, so its bounded waits run out (gemm_kernel.cu).
 void set_gemm_debug_stall(int on);
 
-// GEMM launcher (gemm_kernel.cu).  Arguments are already validated.
+// GEMM launcher (gemm_kernel.cu).  Arguments are already validated.  With
+// amax_out set (a zeroed device float), the epilogue also takes the max |D|
+// over the stored output into it.
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                         cudaStream_t s);
+                         cudaStream_t s, float* amax_out = nullptr);
 
 }  // namespace nvfp4

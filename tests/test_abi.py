@@ -69,6 +69,11 @@ def test_gemm_argument_checks(lib):
     assert call(a, _t(256, 256, codes=24)) == binding.NVFP4_ERR_ARG
     assert call(a, b, d_=ctypes.c_void_p(24)) == binding.NVFP4_ERR_ALIGN
     assert call(a, b, ldd=260) == binding.NVFP4_ERR_ALIGN
+    # the amax variant: its slot is required and 4-byte aligned, then the same checks
+    am = lambda a_, b_, amax_: lib.nvfp4_gemm_amax(ctypes.byref(a_), ctypes.byref(b_), d, 0, 256, amax_, None)
+    assert am(a, b, None) == binding.NVFP4_ERR_ARG
+    assert am(a, b, ctypes.c_void_p(18)) == binding.NVFP4_ERR_ALIGN
+    assert am(_t(100, 256), b, ctypes.c_void_p(16)) == binding.NVFP4_ERR_SHAPE
 
 
 def test_quantize_argument_checks(lib):
@@ -80,6 +85,7 @@ def test_quantize_argument_checks(lib):
     assert q(x_=None) == binding.NVFP4_ERR_ARG
     assert q(r=100) == binding.NVFP4_ERR_SHAPE
     assert q(c=0) == binding.NVFP4_ERR_SHAPE
+    assert q(r=0) == binding.NVFP4_ERR_SHAPE  # empty tensors are not quantized
     assert q(x_=ctypes.c_void_p(8)) == binding.NVFP4_ERR_ALIGN
     assert q(o=_t(128, 128)) == binding.NVFP4_ERR_SHAPE
     assert q(o=_t(64, 256)) == binding.NVFP4_ERR_SHAPE
@@ -97,6 +103,8 @@ def test_linear_argument_checks(lib):
     p = ctypes.c_void_p(16)
     f = lambda M=128, K=256, N=256, wsb=ws, w=p: lib.nvfp4_linear_fwd(p, p, M, K, N, 1, p, w, wsb, None)
     assert f(M=64) == binding.NVFP4_ERR_SHAPE
+    assert f(M=0) == binding.NVFP4_ERR_SHAPE
+    assert f(N=0) == binding.NVFP4_ERR_SHAPE
     assert f(wsb=ws - 1) == binding.NVFP4_ERR_WORKSPACE
     assert f(w=None) == binding.NVFP4_ERR_ARG
     assert f(w=ctypes.c_void_p(8)) == binding.NVFP4_ERR_ALIGN

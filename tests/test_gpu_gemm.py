@@ -131,6 +131,29 @@ def test_strided_bf16_output_pair_kernel(pad):
     assert rel_fro(o[:, :N], ref) <= 1e-3
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 768, 512), (128, 256, 320), (384, 384, 256)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_gemm_output_amax_equals_amax_of_output(M, N, K, out_dtype):
+    """The epilogue's amax of D (both kernels, both output types) is exactly
+    the amax pass over the stored output, and the output itself is the same
+    as without it."""
+    rng = np.random.default_rng(M + N + K)
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    asc = rng.integers(0x28, 0x48, size=(M, K // 16)).astype(np.uint8)
+    bsc = rng.integers(0x28, 0x48, size=(N, K // 16)).astype(np.uint8)
+    qa, qb = make_q(ac, asc, 0.75), make_q(bc, bsc, 1.5)
+    d, amax = B.nvfp4_gemm_amax(qa, qb, out_dtype=out_dtype)
+    plain = B.nvfp4_gemm(qa, qb, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert torch.equal(d, plain)
+    want = float(d.float().abs().max().item())
+    assert amax.item() == want
+    if out_dtype == torch.bfloat16:
+        assert B.nvfp4_amax(d, B.NVFP4_AMAX_PLAIN)[0].item() == want
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+
+
 def test_gemm_repeatable():
     rng = np.random.default_rng(4)
     M, N, K = 256, 512, 768

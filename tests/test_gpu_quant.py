@@ -151,6 +151,17 @@ def test_zero_tensor():
     assert B.nvfp4_get_status() == B.NVFP4_OK
 
 
+def test_empty_tensor_amax():
+    """An empty tensor (no rows) has amax 0 in every slot (the slots are
+    zeroed and nothing is launched), and the status stays clean."""
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((3,), 5.0, dtype=torch.float32, device="cuda")
+    B.nvfp4_amax(x, B.NVFP4_AMAX_PLAIN | B.NVFP4_AMAX_RHT_ROWS | B.NVFP4_AMAX_RHT_COLS, rht_seed=1, out=out)
+    torch.cuda.synchronize()
+    assert out.tolist() == [0.0, 0.0, 0.0]
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+
+
 def test_nonfinite_sets_status():
     x = torch.randn(128, 256).to(torch.bfloat16)
     x[7, 9] = float("inf")
