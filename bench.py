@@ -491,6 +491,98 @@ def run_sweep(args, rank, world, local):
     return 0
 
 
+def time_ms_flushed(fn, stream, flush, reps=5, warm=2):
+    """Mean device time of fn() alone on `stream`, the L2 flushed (a write
+    of `flush`, larger than L2) before every launch."""
+    import torch
+
+    for _ in range(warm):
+        fn()
+    total = 0.0
+    for _ in range(reps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / reps
+
+
+def run_mx(args, rank, world, local):
+    """--mx: the MXFP4 variant of the layer step on the same workload, built
+    from the library's MXFP4 calls: X, W and dY each quantized once to 1x32
+    UE8M0 blocks along both dimensions (rowwise + transposed, RNE), then
+    Y = X W^T, dX = dY W, dW = dY^T X on the tensor cores.  One JSON line
+    with the step time, each part alone (L2 flushed), the quantize kernel's
+    HBM roofline and the GEMM's FP4 roofline, and the NVFP4 GEMM of the same
+    shape for comparison."""
+    import torch
+
+    from nvfp4_bit_numerics_gb300 import binding as B, build as nbuild, workloads
+
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    nbuild.build()
+    B.load_library()
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, bf16_peak, src = measured_peaks()
+    fp4_peak = bf16_peak * FP4_OVER_BF16
+    x, w, dy = (t.to(dev) for t in workloads.mlp_up())
+    qx, qxt = B.empty_mx_qtensor(M, K, device=dev), B.empty_mx_qtensor(K, M, device=dev)
+    qw, qwt = B.empty_mx_qtensor(N, K, device=dev), B.empty_mx_qtensor(K, N, device=dev)
+    qdy, qdyt = B.empty_mx_qtensor(M, N, device=dev), B.empty_mx_qtensor(N, M, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    both = B.NVFP4_Q_ROWWISE_AND_TRANSPOSE
+    parts = {
+        "quant_x": lambda: B.nvfp4_quantize_mx(x, both, out=qx, out_t=qxt, stream=stream),
+        "quant_w": lambda: B.nvfp4_quantize_mx(w, both, out=qw, out_t=qwt, stream=stream),
+        "quant_dy": lambda: B.nvfp4_quantize_mx(dy, both, out=qdy, out_t=qdyt, stream=stream),
+        "gemm_fprop": lambda: B.nvfp4_gemm(qx, qw, out=y, stream=stream),
+        "gemm_dgrad": lambda: B.nvfp4_gemm(qdy, qwt, out=dx, stream=stream),
+        "gemm_wgrad": lambda: B.nvfp4_gemm(qdyt, qxt, out=dw, stream=stream),
+    }
+
+    def step():
+        for f in parts.values():
+            f()
+
+    n0 = B.nvfp4_kernel_launch_count()
+    step()
+    launches = B.nvfp4_kernel_launch_count() - n0
+    ms = time_ms(step, stream, reps=args.steps, warm=args.warmup)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    part_ms = {k: time_ms_flushed(f, stream, flush) for k, f in parts.items()}
+    if B.nvfp4_get_status() != B.NVFP4_OK:
+        raise RuntimeError("device status in the MXFP4 step")
+    # NVFP4 GEMM of the same Fprop shape (operands from the NVFP4 quantizers)
+    nqx = B.empty_qtensor(M, K, device=dev)
+    nqw = B.empty_qtensor(N, K, device=dev)
+    B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE, out=nqx)
+    B.nvfp4_quantize(w, B.NVFP4_Q_2D, out=nqw)
+    nv_ms = time_ms_flushed(lambda: B.nvfp4_gemm(nqx, nqw, out=y, stream=stream), stream, flush)
+    # algorithmic bytes of one fused MXFP4 quantization of an [r, c] tensor:
+    # read 2 B, write two outputs of 0.5 B codes + 1/16 B scale words
+    qbytes = lambda r, c: r * c * (2.0 + 2 * (0.5 + 1.0 / 16))  # noqa: E731
+    dy_gbs = qbytes(M, N) / (part_ms["quant_dy"] * 1e-3) / 1e9
+    gemm_tf = FLOPS_PER_GEMM / (part_ms["gemm_fprop"] * 1e-3) / 1e12
+    print(json.dumps({
+        "mx": "layer", "workload": "mxfp4_linear_fwd_bwd_mlp_up_%dx%dx%d" % (M, K, N),
+        "ms_per_step": ms, "value": FLOPS_PER_STEP / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "gpu_launches_per_step": launches, "parts_ms_l2_flushed": part_ms,
+        "roofline_quant_dy": {"bound": "hbm", "achieved": dy_gbs, "peak": hbm_peak, "unit": "GB/s",
+                              "frac": dy_gbs / hbm_peak, "peak_source": src},
+        "roofline_gemm_fprop": {"bound": "tensor", "achieved": gemm_tf, "peak": fp4_peak, "unit": "TFLOP/s",
+                                "frac": gemm_tf / fp4_peak, "peak_source": src + " bf16 x 6 (nominal fp4:bf16)"},
+        "nvfp4_gemm_fprop_ms_l2_flushed": nv_ms,
+    }), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,6 +591,8 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line, one line per further configured shape")
+    ap.add_argument("--mx", action="store_true",
+                    help="instead of the benchmark line, the MXFP4 variant of the layer step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gpu":
         args.warmup = 3
@@ -507,6 +601,8 @@ def main():
         return run_reference(args, rank, world)
     if args.sweep:
         return run_sweep(args, rank, world, local)
+    if args.mx:
+        return run_mx(args, rank, world, local)
     return run_gpu(args, rank, world, local)
 
 

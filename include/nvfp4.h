@@ -14,6 +14,9 @@
  *     (item 4);
  *   - FP32-accumulated GEMMs on tensor cores that take NVFP4 natively
  *     (Resumo técnico §3, "Suporte de Hardware").
+ * It also quantizes to and multiplies MXFP4, the format the method is
+ * compared with (Resumo técnico §1, "Limitações de Formatos Existentes":
+ * 32-element blocks with power-of-two scales).
  *
  * Conventions shared by every entry point
  *   - All pointers named *_dev or held in nvfp4_tensor are DEVICE pointers on
@@ -63,6 +66,20 @@ enum {
                               block-scaled tensor-core MMA consumes.  Requires
                               rows % 128 == 0 and cols % 64 == 0. */
 };
+/* For an MXFP4 tensor the same two names mean:
+ *   NVFP4_SCALES_LINEAR  row-major [rows, cols/32] UE8M0 bytes;
+ *   NVFP4_SCALES_MMA     the tile layout above with one 4-byte word per 64
+ *                        elements of a row: bytes (E0, E1, 0, 0), E0 the
+ *                        scale of elements 0-31 and E1 of 32-63 -- the bytes
+ *                        a block-scaled MMA with two scales per 64 elements
+ *                        reads.  Same size as the NVFP4 MMA layout. */
+
+/* Element format of an nvfp4_tensor (its `format` field). */
+enum {
+  NVFP4_FORMAT_NVFP4 = 0, /* E2M1, E4M3 scale per 16 elements, FP32 tensor scale */
+  NVFP4_FORMAT_MXFP4 = 1  /* E2M1, UE8M0 scale per 32 elements (value 2^(E-127),
+                             code 255 unused), no tensor scale */
+};
 
 /*
  * A quantized NVFP4 tensor of logical shape [rows, cols]; cols is the
@@ -78,6 +95,10 @@ enum {
  *   tensor_scale  device, 1 float: the FP32 per-tensor decode scale
  *                 ts = 1 / (2688 / amax) (1 when amax == 0), written by
  *                 nvfp4_quantize; value = e2m1(code) * e4m3(scale) * ts.
+ *   format        NVFP4_FORMAT_*; zero (NVFP4) in a zero-initialised struct.
+ *                 An MXFP4 tensor has UE8M0 scales per 32 elements and no
+ *                 amax or tensor scale (both may be NULL):
+ *                 value = e2m1(code) * 2^(scale - 127).
  */
 typedef struct {
   uint8_t* codes;
@@ -87,7 +108,7 @@ typedef struct {
   int64_t rows;
   int64_t cols;
   int32_t scale_layout;
-  int32_t reserved;
+  int32_t format;
 } nvfp4_tensor;
 
 /* What nvfp4_quantize produces. */
@@ -170,7 +191,8 @@ nvfp4_status nvfp4_amax(const void* x_dev, int64_t rows, int64_t cols, int32_t f
  *   out     see nvfp4_quant_cfg.kind for its shape; must match.
  *   out_t   transposed output for the kinds that have one, else ignored.
  * Sizes: rows % 64 == 0 and cols % 64 == 0 (rows, cols > 0); an MMA scale
- * layout also needs its tensor's rows % 128 == 0.
+ * layout also needs its tensor's rows % 128 == 0.  Outputs must have format
+ * NVFP4_FORMAT_NVFP4 (MXFP4 outputs: nvfp4_quantize_mx).
  */
 nvfp4_status nvfp4_quantize(const void* x_dev, int64_t rows, int64_t cols,
                             const nvfp4_quant_cfg* cfg, const nvfp4_tensor* out,
@@ -178,6 +200,31 @@ nvfp4_status nvfp4_quantize(const void* x_dev, int64_t rows, int64_t cols,
 
 /* Bytes of the block-scale tensor of a [rows, cols] NVFP4 tensor. */
 size_t nvfp4_scale_bytes(int64_t rows, int64_t cols, int32_t scale_layout);
+
+/*
+ * nvfp4_quantize_mx -- BF16 -> MXFP4 (Resumo técnico §1, "Limitações de
+ * Formatos Existentes", and §2, "Fatores de Escala Precisos": the format
+ * NVFP4 is compared with).  Scale rule of OCP Microscaling Formats v1.0 for
+ * E2M1, per block of 32 consecutive elements along the blocked dimension:
+ *   E = floor(log2(max |x|)) - 2 + 127, clamped to >= 0 (0 for a zero block);
+ *   code_i = e2m1_rne_satfinite(x_i * 2^(127 - E))  (one float32 multiply).
+ * The block's largest value lands in [4, 8); values above 6 saturate.
+ *   x_dev   BF16 [rows, cols]; finite values (the codes written for a block
+ *           holding inf or NaN are unspecified; nothing is flagged).
+ *   kind    NVFP4_Q_ROWWISE (out = x, blocks along cols), NVFP4_Q_TRANSPOSE
+ *           (out = x^T [cols, rows], blocks along rows) or
+ *           NVFP4_Q_ROWWISE_AND_TRANSPOSE (out = x, out_t = x^T, one read).
+ *   out, out_t  format NVFP4_FORMAT_MXFP4, codes and scales set; amax and
+ *           tensor_scale are ignored.
+ * Sizes: rows % 64 == 0 and cols % 64 == 0 (rows, cols > 0); an MMA scale
+ * layout also needs its tensor's rows % 128 == 0.
+ */
+nvfp4_status nvfp4_quantize_mx(const void* x_dev, int64_t rows, int64_t cols, int32_t kind,
+                               const nvfp4_tensor* out, const nvfp4_tensor* out_t,
+                               nvfp4_stream stream);
+
+/* Bytes of the block-scale tensor of a [rows, cols] MXFP4 tensor. */
+size_t nvfp4_mx_scale_bytes(int64_t rows, int64_t cols, int32_t scale_layout);
 
 enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 };
 
@@ -189,6 +236,9 @@ enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 };
  *   a        [M, K] NVFP4, scales in NVFP4_SCALES_MMA layout.
  *   b        [N, K] NVFP4, scales in NVFP4_SCALES_MMA layout.
  *   d_dev    [M, ldd] BF16 or FP32 (d_dtype = NVFP4_OUT_*), row-major.
+ * With both operands in NVFP4_FORMAT_MXFP4 the same call multiplies MXFP4:
+ * elements decode as e2m1(code) * 2^(scale - 127) with one scale per 32, and
+ * there is no tensor scale.  Mixed formats are rejected (NVFP4_ERR_ARG).
  * Sizes: M % 128 == 0, N % 128 == 0, K % 64 == 0, ldd >= N, and ldd times the
  * element size a multiple of 16 bytes.  M, N or K == 0 is rejected.
  */

@@ -38,12 +38,14 @@ NVFP4_AMAX_RHT_ROWS = 2
 NVFP4_AMAX_RHT_COLS = 4
 NVFP4_OUT_BF16 = 0
 NVFP4_OUT_F32 = 1
+NVFP4_FORMAT_NVFP4 = 0
+NVFP4_FORMAT_MXFP4 = 1
 
 EXPORTED = [
     "nvfp4_amax", "nvfp4_quantize", "nvfp4_scale_bytes", "nvfp4_gemm", "nvfp4_linear_workspace_bytes",
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_linear_get_views", "nvfp4_get_status",
     "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
-    "nvfp4_debug_stall_next_gemm", "nvfp4_gemm_amax",
+    "nvfp4_debug_stall_next_gemm", "nvfp4_gemm_amax", "nvfp4_quantize_mx", "nvfp4_mx_scale_bytes",
 ]
 
 
@@ -56,7 +58,7 @@ class Nvfp4Error(RuntimeError):
 class nvfp4_tensor(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("amax", ctypes.c_void_p),
                 ("tensor_scale", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
-                ("scale_layout", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("scale_layout", ctypes.c_int32), ("format", ctypes.c_int32)]
 
 
 class nvfp4_quant_cfg(ctypes.Structure):
@@ -97,6 +99,8 @@ def load_library(path=LIB_PATH):
         "nvfp4_kernel_launch_count": (U64, []),
         "nvfp4_linear_fwd_noalloc": (I32, [P, P, I64, I64, I64, U64, P, P]),
         "nvfp4_debug_stall_next_gemm": (None, [I32]),
+        "nvfp4_quantize_mx": (I32, [P, I64, I64, I32, T, T, P]),
+        "nvfp4_mx_scale_bytes": (SZ, [I64, I64, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -127,15 +131,18 @@ def _bf16_2d(x, name):
 
 
 class QTensor:
-    """Torch-owned buffers of one NVFP4 tensor [rows, cols] (see nvfp4_tensor)."""
+    """Torch-owned buffers of one quantized tensor [rows, cols] (see
+    nvfp4_tensor); an MXFP4 tensor (fmt NVFP4_FORMAT_MXFP4) has no amax or
+    tensor scale (None)."""
 
-    def __init__(self, codes, scales, amax, tensor_scale, rows, cols, layout):
+    def __init__(self, codes, scales, amax, tensor_scale, rows, cols, layout, fmt=NVFP4_FORMAT_NVFP4):
         self.codes, self.scales, self.amax, self.tensor_scale = codes, scales, amax, tensor_scale
-        self.rows, self.cols, self.layout = rows, cols, layout
+        self.rows, self.cols, self.layout, self.fmt = rows, cols, layout, fmt
 
     def struct(self):
-        return nvfp4_tensor(self.codes.data_ptr(), self.scales.data_ptr(), self.amax.data_ptr(),
-                            self.tensor_scale.data_ptr(), self.rows, self.cols, self.layout, 0)
+        opt = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+        return nvfp4_tensor(self.codes.data_ptr(), self.scales.data_ptr(), opt(self.amax), opt(self.tensor_scale),
+                            self.rows, self.cols, self.layout, self.fmt)
 
 
 def nvfp4_scale_bytes(rows, cols, layout):
@@ -149,6 +156,35 @@ def empty_qtensor(rows, cols, layout=NVFP4_SCALES_MMA, device="cuda"):
     amax = torch.zeros(1, dtype=torch.float32, device=device)
     ts = torch.zeros(1, dtype=torch.float32, device=device)
     return QTensor(codes, scales, amax, ts, rows, cols, layout)
+
+
+def nvfp4_mx_scale_bytes(rows, cols, layout):
+    return int(load_library().nvfp4_mx_scale_bytes(rows, cols, layout))
+
+
+def empty_mx_qtensor(rows, cols, layout=NVFP4_SCALES_MMA, device="cuda"):
+    """Allocate (with torch) the buffers of a [rows, cols] MXFP4 tensor."""
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+    scales = torch.zeros(nvfp4_mx_scale_bytes(rows, cols, layout), dtype=torch.uint8, device=device)
+    return QTensor(codes, scales, None, None, rows, cols, layout, NVFP4_FORMAT_MXFP4)
+
+
+def nvfp4_quantize_mx(x, kind=NVFP4_Q_ROWWISE, out=None, out_t=None, layout=NVFP4_SCALES_MMA, stream=None):
+    """Quantize a BF16 [rows, cols] tensor to MXFP4; returns (out, out_t)
+    QTensors (out_t is None unless kind is NVFP4_Q_ROWWISE_AND_TRANSPOSE)."""
+    _bf16_2d(x, "x")
+    rows, cols = x.shape
+    if out is None:
+        out = empty_mx_qtensor(cols, rows, layout, x.device) if kind == NVFP4_Q_TRANSPOSE else \
+            empty_mx_qtensor(rows, cols, layout, x.device)
+    if out_t is None and kind == NVFP4_Q_ROWWISE_AND_TRANSPOSE:
+        out_t = empty_mx_qtensor(cols, rows, layout, x.device)
+    so = out.struct()
+    st = out_t.struct() if out_t is not None else None
+    _check("nvfp4_quantize_mx", load_library().nvfp4_quantize_mx(
+        _ptr(x), rows, cols, kind, ctypes.byref(so), ctypes.byref(st) if st is not None else None,
+        _stream(stream)))
+    return out, out_t
 
 
 def nvfp4_amax(x, flags=NVFP4_AMAX_PLAIN, rht_seed=0, out=None, stream=None):

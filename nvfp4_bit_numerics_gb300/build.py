@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4.so")
-SOURCES = ["api.cu", "quant_kernels.cu", "gemm_kernel.cu", "static_workspace.cu"]
+SOURCES = ["api.cu", "quant_kernels.cu", "mx_kernels.cu", "gemm_kernel.cu", "static_workspace.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

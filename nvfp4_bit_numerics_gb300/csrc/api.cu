@@ -39,9 +39,13 @@ constexpr uint32_t kStreamDyT = 1;  // stochastic rounding of dY^T (Wgrad operan
 
 nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
+// Codes and scales set and aligned, a known scale layout and format; an
+// NVFP4 tensor also needs its tensor scale.
 bool valid_tensor(const nvfp4_tensor* t) {
-  return t && t->codes && t->scales && t->tensor_scale && aligned16(t->codes) && aligned16(t->scales) &&
-         (t->scale_layout == NVFP4_SCALES_LINEAR || t->scale_layout == NVFP4_SCALES_MMA);
+  if (!t || !t->codes || !t->scales || !aligned16(t->codes) || !aligned16(t->scales)) return false;
+  if (t->scale_layout != NVFP4_SCALES_LINEAR && t->scale_layout != NVFP4_SCALES_MMA) return false;
+  if (t->format == NVFP4_FORMAT_NVFP4) return t->tensor_scale != nullptr;
+  return t->format == NVFP4_FORMAT_MXFP4;
 }
 
 bool layout_ok(const nvfp4_tensor* t) {
@@ -52,6 +56,18 @@ bool layout_ok(const nvfp4_tensor* t) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 152;
+  }
+  return cached[dev];
+}
 
 uint32_t* device_status_ptr() {
   int dev = 0;
@@ -143,7 +159,7 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, const nvf
   if (cfg->kind == NVFP4_Q_ROWWISE_AND_TRANSPOSE && !o_t) return NVFP4_ERR_ARG;
   for (const nvfp4_tensor* t : {o_row, o_t}) {
     if (!t) continue;
-    if (!valid_tensor(t) || !t->amax) return NVFP4_ERR_ARG;
+    if (!valid_tensor(t) || !t->amax || t->format != NVFP4_FORMAT_NVFP4) return NVFP4_ERR_ARG;
     if (!layout_ok(t)) return NVFP4_ERR_SHAPE;
   }
   if (o_row && (o_row->rows != rows || o_row->cols != cols)) return NVFP4_ERR_SHAPE;
@@ -185,9 +201,48 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, const nvf
                                      cfg->seed, cfg->sr_stream, stream_t, s));
 }
 
-nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int32_t d_dtype, int64_t ldd,
-                        nvfp4_stream stream) {
+size_t nvfp4_mx_scale_bytes(int64_t rows, int64_t cols, int32_t layout) {
+  if (rows < 0 || cols < 0) return 0;
+  // the MMA layout pads each pair of 32-element scales to a 4-byte word
+  if (layout == NVFP4_SCALES_MMA) return nvfp4_scale_bytes(rows, cols, layout);
+  return (size_t)(rows * (cols / 32));
+}
+
+nvfp4_status nvfp4_quantize_mx(const void* x, int64_t rows, int64_t cols, int32_t kind, const nvfp4_tensor* out,
+                               const nvfp4_tensor* out_t, nvfp4_stream stream) {
+  if (!x) return NVFP4_ERR_ARG;
+  const nvfp4_tensor* o_row = nullptr;
+  const nvfp4_tensor* o_t = nullptr;
+  switch (kind) {
+    case NVFP4_Q_ROWWISE: o_row = out; break;
+    case NVFP4_Q_TRANSPOSE: o_t = out; break;
+    case NVFP4_Q_ROWWISE_AND_TRANSPOSE:
+      o_row = out;
+      o_t = out_t;
+      if (!o_t) return NVFP4_ERR_ARG;
+      break;
+    default: return NVFP4_ERR_ARG;
+  }
+  if (!o_row && !o_t) return NVFP4_ERR_ARG;
+  if (rows <= 0 || cols <= 0 || rows % 64 || cols % 64) return NVFP4_ERR_SHAPE;
+  if (!aligned16(x)) return NVFP4_ERR_ALIGN;
+  for (const nvfp4_tensor* t : {o_row, o_t}) {
+    if (!t) continue;
+    if (!valid_tensor(t) || t->format != NVFP4_FORMAT_MXFP4) return NVFP4_ERR_ARG;
+    if (!layout_ok(t)) return NVFP4_ERR_SHAPE;
+  }
+  if (o_row && (o_row->rows != rows || o_row->cols != cols)) return NVFP4_ERR_SHAPE;
+  if (o_t && (o_t->rows != cols || o_t->cols != rows)) return NVFP4_ERR_SHAPE;
+  return from_cuda(launch_quant_mx(x, rows, cols, o_row, o_t, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+// Argument checks shared by the GEMM entry points (nothing launched).
+nvfp4_status check_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, const void* d, int32_t d_dtype,
+                        int64_t ldd) {
   if (!valid_tensor(a) || !valid_tensor(b) || !d) return NVFP4_ERR_ARG;
+  if (a->format != b->format) return NVFP4_ERR_ARG;
   if (d_dtype != NVFP4_OUT_BF16 && d_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
   if (a->scale_layout != NVFP4_SCALES_MMA || b->scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_ARG;
   const int64_t M = a->rows, N = b->rows, K = a->cols;
@@ -196,6 +251,15 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, i
   if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return NVFP4_ERR_SHAPE;
   const int64_t esz = d_dtype == NVFP4_OUT_F32 ? 4 : 2;
   if (!aligned16(d) || (ldd * esz) % 16) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int32_t d_dtype, int64_t ldd,
+                        nvfp4_stream stream) {
+  const nvfp4_status st = check_gemm(a, b, d, d_dtype, ldd);
+  if (st != NVFP4_OK) return st;
   return launch_gemm(*a, *b, d, d_dtype, ldd, static_cast<cudaStream_t>(stream));
 }
 
@@ -203,16 +267,8 @@ nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* a, const nvfp4_tensor* b, void*
                              float* amax_dev, nvfp4_stream stream) {
   if (!amax_dev) return NVFP4_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(amax_dev) & 3u) != 0) return NVFP4_ERR_ALIGN;
-  // the same checks as nvfp4_gemm, on a call that launches nothing
-  if (!valid_tensor(a) || !valid_tensor(b) || !d) return NVFP4_ERR_ARG;
-  if (d_dtype != NVFP4_OUT_BF16 && d_dtype != NVFP4_OUT_F32) return NVFP4_ERR_ARG;
-  if (a->scale_layout != NVFP4_SCALES_MMA || b->scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_ARG;
-  const int64_t M = a->rows, N = b->rows, K = a->cols;
-  if (M <= 0 || N <= 0 || K <= 0 || b->cols != K) return NVFP4_ERR_SHAPE;
-  if (M % 128 || N % 128 || K % 64 || ldd < N) return NVFP4_ERR_SHAPE;
-  if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return NVFP4_ERR_SHAPE;
-  const int64_t esz = d_dtype == NVFP4_OUT_F32 ? 4 : 2;
-  if (!aligned16(d) || (ldd * esz) % 16) return NVFP4_ERR_ALIGN;
+  const nvfp4_status st = check_gemm(a, b, d, d_dtype, ldd);
+  if (st != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(amax_dev, 0, sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
   return launch_gemm(*a, *b, d, d_dtype, ldd, s, amax_dev);
@@ -263,7 +319,7 @@ void fill_views(uint8_t* ws, int64_t M, int64_t K, int64_t N, nvfp4_linear_views
     t[i]->rows = L.rows[i];
     t[i]->cols = L.cols[i];
     t[i]->scale_layout = NVFP4_SCALES_MMA;
-    t[i]->reserved = 0;
+    t[i]->format = NVFP4_FORMAT_NVFP4;
   }
 }
 

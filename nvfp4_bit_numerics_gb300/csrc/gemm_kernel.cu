@@ -2,6 +2,17 @@
 //
 //   D[M, N] = ts_a * ts_b * sum_k e2m1(A[m,k]) e4m3(SA[m,k/16]) e2m1(B[n,k]) e4m3(SB[n,k/16])
 //
+// and, for MXFP4 operands (Params::mx; Resumo técnico §1, the 32-element,
+// power-of-two-scaled format NVFP4 is compared with),
+//
+//   D[M, N] = sum_k e2m1(A[m,k]) 2^(SA[m,k/32]-127) e2m1(B[n,k]) 2^(SB[n,k/32]-127)
+//
+// with tcgen05.mma.kind::mxf4.block_scale.scale_vec::2X and UE8M0 scales.  The
+// MXFP4 scales arrive in the same 512-byte tiles as the NVFP4 ones, each
+// 4-byte word holding the two scales of a 64-element K chunk in bytes 0 and 1
+// (the bytes the 2X MMA reads with scale-factor id 0), so everything but the
+// MMA instruction and its descriptor is shared.
+//
 // The GEMMs of "Pretraining Large Language Models with NVFP4" (gist.science
 // summary), Resumo técnico §3 ("Suporte de Hardware": Blackwell tensor cores
 // take NVFP4 natively) -- Fprop, Dgrad and Wgrad of a linear layer, each a
@@ -40,6 +51,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -90,6 +102,7 @@ struct Params {
   int debug_stall; // failure-detection test: the first stage's loads are never issued
   int tma_store;   // pair kernel: BF16 output written by bulk tensor stores
   uint32_t* amax_out;  // if set: max |D| over the stored output, as float bits (atomicMax)
+  int mx;              // operands are MXFP4 (UE8M0 scales per 32, no tensor scales)
   uint32_t* status;
 };
 
@@ -196,9 +209,21 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same for MXFP4 operands: bit 23 selects UE8M0 scales.
+__host__ __device__ constexpr uint32_t idesc_block_scaled(int M, int N, bool mx) {
+  return idesc_mxf4nvf4(M, N) | (mx ? (1u << 23) : 0u);
+}
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                                       uint32_t accumulate) {
+                                       uint32_t accumulate, bool mx) {
+  if (mx)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -359,8 +384,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ----------------------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_mxf4nvf4(kBM, BN);
+    // The loop is instantiated once per operand format, so the MMA issue path
+    // carries no format test (a per-MMA branch slowed it by a quarter).
+    auto issue = [&](auto mx_tag) {
+      constexpr bool kMX = decltype(mx_tag)::value;
+      const uint32_t idesc = idesc_block_scaled(kBM, BN, kMX);
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -377,7 +405,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           uint32_t sfa = tmem + (uint32_t)(stage * C::kSfStageCols + C::kSfaCol);
           uint32_t sfb = tmem + (uint32_t)(stage * C::kSfStageCols + C::kSfbCol);
           for (int j = 0; j < nk; ++j) {
-            tc_mma(tmem, da, db, idesc, sfa, sfb, (ks | j) != 0);
+            tc_mma(tmem, da, db, idesc, sfa, sfb, (ks | j) != 0, kMX);
             da += 2;  // +32 bytes along K inside the 128-byte swizzle atom
             db += 2;
             sfa += 4;
@@ -390,6 +418,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_commit(tmem_full);
         acc_phase ^= 1u;
       }
+    };
+    if (lane == 0) {
+      if (p.mx) issue(std::true_type{});
+      else issue(std::false_type{});
       // all MMAs and copies issued by this thread have finished
       tc_commit(mma_done);
       volatile int never = 0;
@@ -447,7 +479,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;
     const int half = (warp - kFirstEpiWarp) >> 2;
-    const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    const float alpha = p.mx ? 1.0f : __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       int mb, nb;
@@ -611,7 +643,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 }
 
 __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                            uint32_t sfb, uint32_t accumulate) {
+                                            uint32_t sfb, uint32_t accumulate, bool mx) {
+  if (mx)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -751,8 +791,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer (even CTA) ------------------
-    if (rank == 0 && lane == 0) {
-      const uint32_t idesc = idesc_mxf4nvf4(256, kPairBN);
+    // one instantiation per operand format, as in the single-CTA kernel
+    auto issue = [&](auto mx_tag) {
+      constexpr bool kMX = decltype(mx_tag)::value;
+      const uint32_t idesc = idesc_block_scaled(256, kPairBN, kMX);
       int stage = 0, region = 0;
       uint32_t phase = 0, rphase = 0, acc_phase = 0;
       bool ok = true;
@@ -768,7 +810,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           uint64_t da = desc_sw128(sa), db = desc_sw128(sa + kPairABytes);
           uint32_t sfa = tmem + (uint32_t)(kPairBN + region * kPairSfCols), sfb = sfa + 16;
           for (int j = 0; j < nk; ++j) {
-            tc_mma_pair(tmem, da, db, idesc, sfa, sfb, (ks | j) != 0);
+            tc_mma_pair(tmem, da, db, idesc, sfa, sfb, (ks | j) != 0, kMX);
             da += 2;  // +32 bytes along K inside the 128-byte swizzle atom
             db += 2;
             sfa += 4;
@@ -782,6 +824,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         tc_commit_pair_multicast(tmem_full);
         acc_phase ^= 1u;
       }
+    };
+    if (rank == 0 && lane == 0) {
+      if (p.mx) issue(std::true_type{});
+      else issue(std::false_type{});
       tc_commit_pair(mma_done);
       volatile int never = 0;
       mbar_wait(mma_done, 0, &never, p.status);
@@ -845,7 +891,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const int q = warp & 3;
     const int half = (warp - kFirstEpiWarp) >> 2;
     constexpr int kCols = kPairBN / 2;
-    const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    const float alpha = p.mx ? 1.0f : __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < n_tiles; tile += num_pairs) {
       int mb, nb;
@@ -976,18 +1022,7 @@ bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 152;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 152;
-  }
-  return cached[dev];
-}
+int sm_count() { return device_sm_count(); }
 
 template <int BN>
 nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
@@ -1023,6 +1058,7 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
   p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
   p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
+  p.mx = a.format == NVFP4_FORMAT_MXFP4;
   p.tma_store = 0;
   const int tiles = (p.M / kBM) * (p.N / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
@@ -1064,6 +1100,7 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   p.debug_stall = g_debug_stall.exchange(0);
   p.status = device_status_ptr();
   p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
+  p.mx = a.format == NVFP4_FORMAT_MXFP4;
   // BF16 output goes through bulk tensor stores (the API guarantees the
   // 16-byte aligned base and row stride they need); FP32 through plain stores
   CUtensorMap md = ma;  // unused for FP32 output

@@ -26,6 +26,10 @@ inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_o
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Number of SMs of the current device (cached per device; 152 if the query
+// fails).
+int device_sm_count();
+
 // Quantize launchers (quant_kernels.cu).  Arguments are already validated.
 // Each non-null output is zeroed and then receives its amax: max|x|, max|Qx|
 // with Q along the contiguous dimension, max|Qx| with Q along rows.
@@ -40,6 +44,12 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
                               cudaStream_t s);
 cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvfp4_tensor& out,
                             const nvfp4_tensor* out_t, const float* amax, cudaStream_t s);
+
+// MXFP4 quantization (mx_kernels.cu): x [rows, cols] BF16 -> out_row
+// [rows, cols] and/or out_t [cols, rows], 1x32 blocks, UE8M0 scales, RNE.
+// Arguments are already validated (rows % 64 == 0, cols % 64 == 0).
+cudaError_t launch_quant_mx(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor* out_row,
+                            const nvfp4_tensor* out_t, cudaStream_t s);
 
 // Failure-detection test hook: the next GEMM launch never issues its first
 // stage's loads, so its bounded waits run out (gemm_kernel.cu).

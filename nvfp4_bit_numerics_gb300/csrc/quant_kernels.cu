@@ -28,18 +28,7 @@ constexpr int kThreads = 256;
 // or more (over 2^42 elements).
 constexpr int64_t kMaxUnits = int64_t(1) << 31;
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 152;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 152;
-  }
-  return cached[dev];
-}
+int sm_count() { return device_sm_count(); }
 
 int grid_for(int64_t units, int per_sm) {
   const int64_t cap = (int64_t)sm_count() * per_sm;

@@ -48,10 +48,17 @@ def test_size_queries(lib):
     elems = 2 * 128 * 256 + 2 * 256 * 256 + 2 * 256 * 128
     assert ws >= elems * 0.5625 + 256
     assert binding.nvfp4_linear_workspace_bytes(0, 1, 1) == 0
+    # MXFP4: one byte per 32 elements, or the padded words of the tile layout
+    assert binding.nvfp4_mx_scale_bytes(100, 64, binding.NVFP4_SCALES_LINEAR) == 200
+    assert binding.nvfp4_mx_scale_bytes(128, 256, binding.NVFP4_SCALES_MMA) == 128 * 16
 
 
-def _t(rows, cols, layout=1, codes=16, scales=16, amax=16, ts=16):
-    return binding.nvfp4_tensor(codes, scales, amax, ts, rows, cols, layout, 0)
+def _t(rows, cols, layout=1, codes=16, scales=16, amax=16, ts=16, fmt=0):
+    return binding.nvfp4_tensor(codes, scales, amax, ts, rows, cols, layout, fmt)
+
+
+def _mx(rows, cols, layout=1, codes=16, scales=16):
+    return _t(rows, cols, layout, codes, scales, None, None, binding.NVFP4_FORMAT_MXFP4)
 
 
 def test_gemm_argument_checks(lib):
@@ -74,6 +81,38 @@ def test_gemm_argument_checks(lib):
     assert am(a, b, None) == binding.NVFP4_ERR_ARG
     assert am(a, b, ctypes.c_void_p(18)) == binding.NVFP4_ERR_ALIGN
     assert am(_t(100, 256), b, ctypes.c_void_p(16)) == binding.NVFP4_ERR_SHAPE
+    # formats: an NVFP4 tensor needs its tensor scale, an MXFP4 one does not;
+    # mixed formats and unknown formats are rejected
+    assert call(_t(128, 256, ts=None), b) == binding.NVFP4_ERR_ARG
+    assert call(_mx(128, 256), _t(256, 256)) == binding.NVFP4_ERR_ARG
+    assert call(_t(128, 256, fmt=2), _t(256, 256, fmt=2)) == binding.NVFP4_ERR_ARG
+    assert call(_mx(100, 256), _mx(256, 256)) == binding.NVFP4_ERR_SHAPE
+    assert call(_mx(128, 256, layout=0), _mx(256, 256)) == binding.NVFP4_ERR_ARG
+
+
+def test_quantize_mx_argument_checks(lib):
+    x = ctypes.c_void_p(16)
+    out, out_t = _mx(128, 256), _mx(256, 128)
+    q = lambda x_=x, r=128, c=256, k=0, o=out, ot=None: lib.nvfp4_quantize_mx(
+        x_, r, c, k, ctypes.byref(o) if o is not None else None, ctypes.byref(ot) if ot is not None else None, None)
+    assert q(x_=None) == binding.NVFP4_ERR_ARG
+    assert q(k=3) == binding.NVFP4_ERR_ARG          # no 2D kind for MXFP4
+    assert q(k=-1) == binding.NVFP4_ERR_ARG
+    assert q(o=None) == binding.NVFP4_ERR_ARG
+    assert q(k=2) == binding.NVFP4_ERR_ARG          # fused kind needs out_t
+    assert q(o=_t(128, 256)) == binding.NVFP4_ERR_ARG  # an NVFP4 output
+    assert q(r=100) == binding.NVFP4_ERR_SHAPE
+    assert q(c=96) == binding.NVFP4_ERR_SHAPE
+    assert q(r=0) == binding.NVFP4_ERR_SHAPE
+    assert q(x_=ctypes.c_void_p(8)) == binding.NVFP4_ERR_ALIGN
+    assert q(o=_mx(128, 128)) == binding.NVFP4_ERR_SHAPE
+    assert q(k=1) == binding.NVFP4_ERR_SHAPE        # transposed output must be [256, 128]
+    assert q(r=64, c=256, o=_mx(64, 256)) == binding.NVFP4_ERR_SHAPE  # MMA layout needs rows % 128
+    assert q(o=_mx(128, 256, codes=24)) == binding.NVFP4_ERR_ARG
+    # and nvfp4_quantize refuses MXFP4 outputs
+    cfg = binding.nvfp4_quant_cfg(0, 0, 0, 0, 0, 0, 0)
+    mxo = _t(128, 256, fmt=binding.NVFP4_FORMAT_MXFP4)
+    assert lib.nvfp4_quantize(x, 128, 256, ctypes.byref(cfg), ctypes.byref(mxo), None, None) == binding.NVFP4_ERR_ARG
 
 
 def test_quantize_argument_checks(lib):
