@@ -48,11 +48,10 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
-#include <cstring>
 #include <atomic>
-#include <mutex>
 #include <type_traits>
 
+#include "device_async.cuh"
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -67,7 +66,6 @@ constexpr int kNumThreads = 448;  // 14 warps
 constexpr int kEpiWarps = 8;
 constexpr int kSfWarps = 4;
 constexpr int kFirstEpiWarp = 6;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 template <int BN>
 struct Cfg {
@@ -117,77 +115,6 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     mb = tile % num_m;
     nb = tile / num_m;
   }
-}
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: true when the phase with `parity` completed; false if the
-// kernel is aborting or the wait exceeded kTimeoutNs (which starts the abort).
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
-        *abort = 1;
-        raise_status(status, kStatusTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-// Fast path inline (one try_wait); the bounded spin lives out of line.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status) {
-  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort, status);
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -981,23 +908,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 // ---------------------------------------------------------------------------
 std::atomic<int> g_debug_stall{0};
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
 // 2D map over packed codes: inner dimension = row bytes, box = 128 B x box_rows.
 bool make_code_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
@@ -1011,7 +924,7 @@ bool make_code_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_
 // 2D map over a BF16 [rows, cols] output with row stride ld elements; box =
 // 16 columns x 32 rows, 32-byte swizzle (the epilogue's staging layout).
 bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {ld * 2};

@@ -1,6 +1,8 @@
 // internal.h -- declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -25,6 +27,10 @@ extern std::atomic<uint64_t> g_launches;
 inline void count_launch(uint64_t n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled of the driver, resolved once (nullptr if the driver
+// does not provide it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn();
 
 // Number of SMs of the current device (cached per device; 152 if the query
 // fails).

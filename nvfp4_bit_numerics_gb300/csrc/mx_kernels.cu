@@ -18,30 +18,47 @@
 // falls below 2^-126, where it is far below the first rounding threshold
 // (0.25) of E2M1.
 //
-// The kernel is bound by HBM bandwidth: 2 bytes read per element, 0.5 + 1/32
-// bytes written per element and output.  One read of a 128 x 64 tile, staged
-// in shared memory, feeds the rowwise output (threads 0-127, one 64-element
-// row chunk each) and the transposed output (threads 128-255, one 64-row
-// column chunk each), so every thread writes whole 32-byte code runs and one
-// whole scale word.
+// The kernel is bound by HBM bandwidth: 2 bytes read per element, 0.5 + 1/16
+// bytes written per element and output (codes and MMA-layout scale words).
+// It is a persistent TMA pipeline: a producer warp streams 128 x 64 BF16
+// tiles (16 KB, 128-byte swizzle) into a 4-slot shared-memory ring with
+// cp.async.bulk.tensor, and 8 consumer warps encode each tile once it has
+// landed -- threads 0-127 one 64-element row chunk each (rowwise output),
+// threads 128-255 one 64-row column chunk each (transposed output) -- so
+// every thread writes whole 32-byte code runs and one whole scale word while
+// the next tiles are already in flight.  The swizzle (16-byte chunk j of row
+// r stored at chunk j ^ (r % 8)) makes both the row reads (8 rows per
+// 16-byte load phase) and the column reads (32 columns of one row) free of
+// shared-memory bank conflicts.
 #include <cuda_runtime.h>
 
+#include "device_async.cuh"
 #include "device_common.cuh"
 #include "internal.h"
 
 namespace nvfp4 {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
 constexpr int kRowsPerTile = 128;
 constexpr int kColsPerTile = 64;
-constexpr int kPitch = 72;  // uint16 per shared-memory row: 144 B, conflict-free 16-byte row reads
+constexpr int kTileBytes = kRowsPerTile * kColsPerTile * 2;
+constexpr int kStages = 4;
+constexpr int kSmemBytes = kStages * kTileBytes + 1024;  // + alignment of the ring to 1024 B
+constexpr int kCtasPerSm = 3;
 constexpr int64_t kMaxTiles = int64_t(1) << 31;
 
 struct MxOut {
   uint8_t* codes;
   uint8_t* scales;
   int layout;
+};
+
+struct MxParams {
+  int64_t rows, cols;
+  MxOut orow, ot;
+  uint32_t* status;
 };
 
 // UE8M0 code of a block whose max |x| has the BF16 bits `amax16` (sign clear,
@@ -53,12 +70,23 @@ __device__ __forceinline__ uint32_t mx_scale(uint32_t amax16, float& mult) {
   return E;
 }
 
+// a *= m, b *= m: two IEEE round-to-nearest float32 multiplies in one packed
+// instruction.
+__device__ __forceinline__ void mul2_rn(float& a, float& b, float m) {
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 y, {%2, %2};\n\t"
+      "mul.rn.f32x2 x, x, y;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(m));
+}
+
 // 32 values -> 16 bytes of codes (element 2j in the low nibble of byte j).
-__device__ __forceinline__ uint4 mx_encode32(const float* v, float mult) {
-  float s[32];
+__device__ __forceinline__ uint4 mx_encode32(float* v, float mult) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) s[i] = __fmul_rn(v[i], mult);
-  return make_uint4(e2m1x8_rn(s), e2m1x8_rn(s + 8), e2m1x8_rn(s + 16), e2m1x8_rn(s + 24));
+  for (int i = 0; i < 32; i += 2) mul2_rn(v[i], v[i + 1], mult);
+  return make_uint4(e2m1x8_rn(v), e2m1x8_rn(v + 8), e2m1x8_rn(v + 16), e2m1x8_rn(v + 24));
 }
 
 // Scale word of the 64-element chunk `chunk` of row r: in the MMA layout the
@@ -73,106 +101,251 @@ __device__ __forceinline__ void mx_store_scales(const MxOut& o, int64_t r, int64
     *reinterpret_cast<uint16_t*>(o.scales + r * (cols >> 5) + 2 * chunk) = (uint16_t)(E0 | (E1 << 8));
 }
 
-template <bool kRow, bool kT>
-__global__ void __launch_bounds__(kThreads, 4) mx_quant_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                                    int64_t cols, MxOut orow, MxOut ot) {
-  __shared__ __align__(16) uint16_t tile[kRowsPerTile * kPitch];
-  const int t = threadIdx.x;
-  const uint32_t tiles_c = (uint32_t)(cols / kColsPerTile);
-  const uint32_t n_tiles = (uint32_t)((rows + kRowsPerTile - 1) / kRowsPerTile) * tiles_c;  // < 2^31 (launcher)
-  for (uint32_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x) {
-    const uint32_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
-    const int64_t m0 = (int64_t)tm * kRowsPerTile, c0 = (int64_t)tc * kColsPerTile;
-    const int valid = rows - m0 < kRowsPerTile ? (int)(rows - m0) : kRowsPerTile;  // 64 or 128
-    uint4 q[4];
+// Shared-memory offsets.  A tile is 128 rows of 128 bytes with the 128-byte
+// swizzle: 16-byte chunk j of row r is stored at chunk j ^ (r % 8).  Each
+// consumer thread keeps its role for the whole kernel, so the eight offsets
+// it reads from are computed once; every load is then the tile base plus a
+// precomputed offset plus a constant.
+//
+// Rowwise thread r: off[j] = byte offset of chunk j (elements 8j .. 8j+7) of
+// row r.
+__device__ __forceinline__ void row_offsets(int r, uint32_t* off) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int v = t + k * kThreads;  // row v/8, 8-element piece v%8
-      q[k] = (v >> 3) < valid ? ldg_nc_v4(x + (m0 + (v >> 3)) * cols + c0 + (v & 7) * 8) : make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();  // the previous tile's readers are done
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int v = t + k * kThreads;
-      *reinterpret_cast<uint4*>(&tile[(v >> 3) * kPitch + (v & 7) * 8]) = q[k];
-    }
-    __syncthreads();
+  for (int j = 0; j < 8; ++j) off[j] = (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4));
+}
 
-    if (t < 128) {
-      if (kRow && t < valid) {
-        const int64_t gr = m0 + t;
-        uint32_t E[2];
-        uint4 o[2];
+// Transposed thread u (0..127): the column pair (2 cp, 2 cp + 1) over the 32
+// rows 32 rb .. 32 rb + 31, where rb % 2 = u % 2 (so the two 32-row blocks of
+// a 64-element scale word sit in neighbouring lanes).  The odd lane reads its
+// rows in the order i ^ 4, so that in every step the warp's two row sets fall
+// on different swizzle chunks (no bank conflicts): row i of its block is at
+// off[(i % 8) ^ order] + 1024 (i / 8) with order = 4 (u % 2).
+struct ColRole {
+  int rb, cp;
+  uint32_t rot;  // 16 for the odd lane: rotates its code words back to row order
+};
+__device__ __forceinline__ ColRole col_role(int u, uint32_t* off) {
+  ColRole c;
+  const int rb_lo = u & 1, order = rb_lo << 2;
+  c.rb = ((u >> 6) << 1) | rb_lo;
+  c.cp = ((u >> 1) & 15) | (((u >> 5) & 1) << 4);
+  c.rot = (uint32_t)order << 2;
+  const int cq = c.cp >> 2, cw = (c.cp & 3) * 4;  // chunk and byte of column 2 cp
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const uint4* sp = reinterpret_cast<const uint4*>(&tile[t * kPitch + 32 * b]);
-          uint4 w[4];
-          uint32_t m = 0;
+  for (int k = 0; k < 8; ++k) {
+    const int ko = k ^ order;  // row within the 8-row group = its swizzle phase
+    off[k] = (uint32_t)((32 * c.rb + ko) * 128 + (((cq ^ ko) & 7) << 4) + cw);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Eight BF16 values (the low or high halves of eight words) -> one word of
+// E2M1 codes, scaled by mult.
+template <bool kHigh>
+__device__ __forceinline__ uint32_t encode8_halves(const uint32_t* w, float mult) {
+  float v[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            w[i] = sp[i];
-            m = __vmaxu2(m, __vmaxu2(__vmaxu2(w[i].x & 0x7FFF7FFFu, w[i].y & 0x7FFF7FFFu),
-                                     __vmaxu2(w[i].z & 0x7FFF7FFFu, w[i].w & 0x7FFF7FFFu)));
-          }
-          float mult;
-          E[b] = mx_scale(max(m & 0xFFFFu, m >> 16), mult);
-          float v[32];
+  for (int i = 0; i < 8; ++i) v[i] = kHigh ? bf16hi(w[i]) : bf16lo(w[i]);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) unpack8(w[i], v + 8 * i);
-          o[b] = mx_encode32(v, mult);
-        }
-        uint4* cp = reinterpret_cast<uint4*>(orow.codes + gr * (cols >> 1) + (c0 >> 1));
-        cp[0] = o[0];
-        cp[1] = o[1];
-        mx_store_scales(orow, gr, c0 >> 6, cols, E[0], E[1]);
+  for (int i = 0; i < 8; i += 2) mul2_rn(v[i], v[i + 1], mult);
+  return e2m1x8_rn(v);
+}
+
+// Rowwise output: row r (< valid) of the tile, 64 elements from column c0.
+__device__ __forceinline__ void encode_row(uint32_t tile, const uint32_t* off, int64_t gr, int64_t c0,
+                                           int64_t cols, const MxOut& o) {
+  uint32_t E[2];
+  uint4 out[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    uint4 w[4];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[i] = lds128(tile + off[4 * b + i]);
+      m = __vmaxu2(m, __vmaxu2(__vmaxu2(w[i].x & 0x7FFF7FFFu, w[i].y & 0x7FFF7FFFu),
+                               __vmaxu2(w[i].z & 0x7FFF7FFFu, w[i].w & 0x7FFF7FFFu)));
+    }
+    float mult;
+    E[b] = mx_scale(max(m & 0xFFFFu, m >> 16), mult);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) unpack8(w[i], v + 8 * i);
+    out[b] = mx_encode32(v, mult);
+  }
+  uint4* cp = reinterpret_cast<uint4*>(o.codes + gr * (cols >> 1) + (c0 >> 1));
+  cp[0] = out[0];
+  cp[1] = out[1];
+  mx_store_scales(o, gr, c0 >> 6, cols, E[0], E[1]);
+}
+
+// Transposed output of one thread (see ColRole): rows gr = c0 + 2 cp and
+// gr + 1 of x^T, columns gm = m0 + 32 rb .. gm + 31, one 32-bit word (both
+// columns) read per row.
+__device__ __forceinline__ void encode_cols(uint32_t tile, const uint32_t* off, const ColRole& c,
+                                            int64_t m0, int64_t c0, int64_t rows, const MxOut& o) {
+  uint32_t w[32];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    w[i] = lds32(tile + off[i & 7] + 1024 * (i >> 3));
+    m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  }
+  float ma, mb;
+  const uint32_t Ea = mx_scale(m & 0xFFFFu, ma), Eb = mx_scale(m >> 16, mb);
+  uint32_t ca[4], cb[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ca[k] = encode8_halves<false>(w + 8 * k, ma);
+    cb[k] = encode8_halves<true>(w + 8 * k, mb);
+    ca[k] = __funnelshift_l(ca[k], ca[k], c.rot);
+    cb[k] = __funnelshift_l(cb[k], cb[k], c.rot);
+  }
+  const int64_t gr = c0 + 2 * c.cp, gm = m0 + 32 * c.rb;
+  *reinterpret_cast<uint4*>(o.codes + gr * (rows >> 1) + (gm >> 1)) = make_uint4(ca[0], ca[1], ca[2], ca[3]);
+  *reinterpret_cast<uint4*>(o.codes + (gr + 1) * (rows >> 1) + (gm >> 1)) = make_uint4(cb[0], cb[1], cb[2], cb[3]);
+  // even lane: column 2cp's word (own Ea, partner's Ea); odd lane: column
+  // 2cp+1's word (partner's Eb, own Eb)
+  const bool odd = c.rb & 1;
+  const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, odd ? Ea : Eb, 1);
+  if (odd)
+    mx_store_scales(o, gr + 1, gm >> 6, rows, other, Eb);
+  else
+    mx_store_scales(o, gr, gm >> 6, rows, Ea, other);
+}
+
+template <bool kRow, bool kT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) mx_quant_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                        MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * kStages];  // full[s], empty[s]
+  __shared__ int abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms are 1024 B
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
+  volatile int* abort = &abort_flag;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  if (t == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kConsumerWarps);
+    }
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const uint32_t tiles_c = (uint32_t)(p.cols / kColsPerTile);
+  const uint32_t n_tiles = (uint32_t)((p.rows + kRowsPerTile - 1) / kRowsPerTile) * tiles_c;  // < 2^31
+  if (warp == kConsumerWarps) {
+    // ---- producer: one lane streams this CTA's tiles into the ring ----
+    if (lane == 0) {
+      int n = 0;
+      for (uint32_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x, ++n) {
+        const int s = n % kStages;
+        if (n >= kStages && !mbar_wait(empty_bar(s), (uint32_t)((n / kStages) - 1) & 1u, abort, p.status)) break;
+        const uint32_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
+        mbar_arrive_expect_tx(full_bar(s), kTileBytes);
+        tma_load_2d(ring + (uint32_t)s * kTileBytes, &xmap, (int)(tc * kColsPerTile), (int)(tm * kRowsPerTile),
+                    full_bar(s));
       }
-    } else if (kT) {
-      const int u = t - 128, c = u & 63, h = u >> 6;  // tile column, 64-row half
-      if (64 * h < valid) {
-        const int64_t gr = c0 + c, gm = m0 + 64 * h;  // row and first column of the transposed tensor
-        uint32_t E[2];
-        uint4 o[2];
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          float v[32];
-          uint32_t m = 0;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const uint32_t w = tile[(64 * h + 32 * b + i) * kPitch + c];
-            m = max(m, w & 0x7FFFu);
-            v[i] = __uint_as_float(w << 16);
-          }
-          float mult;
-          E[b] = mx_scale(m, mult);
-          o[b] = mx_encode32(v, mult);
-        }
-        uint4* cp = reinterpret_cast<uint4*>(ot.codes + gr * (rows >> 1) + (gm >> 1));
-        cp[0] = o[0];
-        cp[1] = o[1];
-        mx_store_scales(ot, gr, gm >> 6, rows, E[0], E[1]);
+      // every load this CTA issued has landed before it exits: the last
+      // kStages loads' phases (the earlier ones were consumed), each wait
+      // bounded and independent of the abort flag
+      volatile int never = 0;
+      for (int k = n - kStages > 0 ? n - kStages : 0; k < n; ++k)
+        mbar_wait(full_bar(k % kStages), (uint32_t)(k / kStages) & 1u, &never, p.status);
+    }
+  } else {
+    // ---- consumers: threads 0-127 rowwise, 128-255 transposed ----
+    uint32_t off[8];
+    ColRole col{};
+    if (t < 128) row_offsets(t, off);
+    else col = col_role(t - 128, off);
+    int n = 0;
+    for (uint32_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x, ++n) {
+      const int s = n % kStages;
+      if (!mbar_wait(full_bar(s), (uint32_t)(n / kStages) & 1u, abort, p.status)) break;
+      const uint32_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
+      const int64_t m0 = (int64_t)tm * kRowsPerTile, c0 = (int64_t)tc * kColsPerTile;
+      const int valid = p.rows - m0 < kRowsPerTile ? (int)(p.rows - m0) : kRowsPerTile;  // 64 or 128
+      const uint32_t tile = ring + (uint32_t)s * kTileBytes;
+      if (t < 128) {
+        if (kRow && t < valid) encode_row(tile, off, m0 + t, c0, p.cols, p.orow);
+      } else if (kT) {
+        if (64 * (col.rb >> 1) < valid) encode_cols(tile, off, col, m0, c0, p.rows, p.ot);  // warp-uniform
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
     }
   }
+  __syncthreads();
+}
+
+// 2D map over x [rows, cols] BF16: box 64 columns x 128 rows, 128-byte
+// swizzle; rows past the end of x read as zeros.
+bool make_x_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols) {
+  auto fn = tensor_map_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {kColsPerTile, kRowsPerTile};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kRow, bool kT>
+cudaError_t launch(const CUtensorMap& map, const MxParams& p, unsigned grid, cudaStream_t s) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(mx_quant_kernel<kRow, kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  mx_quant_kernel<kRow, kT><<<grid, kThreads, kSmemBytes, s>>>(map, p);
+  count_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quant_mx(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor* out_row,
                             const nvfp4_tensor* out_t, cudaStream_t s) {
-  MxOut orow{}, ot{};
-  if (out_row) orow = MxOut{out_row->codes, out_row->scales, out_row->scale_layout};
-  if (out_t) ot = MxOut{out_t->codes, out_t->scales, out_t->scale_layout};
+  MxParams p{};
+  p.rows = rows;
+  p.cols = cols;
+  if (out_row) p.orow = MxOut{out_row->codes, out_row->scales, out_row->scale_layout};
+  if (out_t) p.ot = MxOut{out_t->codes, out_t->scales, out_t->scale_layout};
+  p.status = device_status_ptr();
   const int64_t tiles = ((rows + kRowsPerTile - 1) / kRowsPerTile) * (cols / kColsPerTile);
   if (tiles >= kMaxTiles) return cudaErrorInvalidValue;
   if (tiles == 0) return cudaSuccess;
-  const int64_t cap = (int64_t)device_sm_count() * 4;
+  CUtensorMap map;
+  if (!make_x_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
+  const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
   const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
-  const uint16_t* xp = static_cast<const uint16_t*>(x);
-  if (out_row && out_t) mx_quant_tile_kernel<true, true><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot);
-  else if (out_t) mx_quant_tile_kernel<false, true><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot);
-  else mx_quant_tile_kernel<true, false><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot);
-  count_launch();
-  return cudaGetLastError();
+  if (out_row && out_t) return launch<true, true>(map, p, grid, s);
+  if (out_t) return launch<false, true>(map, p, grid, s);
+  return launch<true, false>(map, p, grid, s);
 }
 
 }  // namespace nvfp4
