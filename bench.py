@@ -510,14 +510,11 @@ def time_ms_flushed(fn, stream, flush, reps=5, warm=2):
     return total / reps
 
 
-def run_mx(args, rank, world, local):
-    """--mx: the MXFP4 variant of the layer step on the same workload, built
-    from the library's MXFP4 calls: X, W and dY each quantized once to 1x32
-    UE8M0 blocks along both dimensions (rowwise + transposed, RNE), then
-    Y = X W^T, dX = dY W, dW = dY^T X on the tensor cores.  One JSON line
-    with the step time, each part alone (L2 flushed), the quantize kernel's
-    HBM roofline and the GEMM's FP4 roofline, and the NVFP4 GEMM of the same
-    shape for comparison."""
+def run_next(args, rank, world, local):
+    """--next: one JSON line per further path built on the same workload:
+    (1) the GEMM epilogue's output amax (nvfp4_gemm_amax) against the plain
+    GEMM plus a separate amax pass over its output; (2) the MXFP4 variant of
+    the layer step; (3) the layer step of a layer kept in BF16."""
     import torch
 
     from nvfp4_bit_numerics_gb300 import binding as B, build as nbuild, workloads
@@ -531,6 +528,26 @@ def run_mx(args, rank, world, local):
     hbm_peak, bf16_peak, src = measured_peaks()
     fp4_peak = bf16_peak * FP4_OVER_BF16
     x, w, dy = (t.to(dev) for t in workloads.mlp_up())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    # (1) NEXT-1: the output amax taken in the GEMM epilogue
+    nqx = B.empty_qtensor(M, K, device=dev)
+    nqw = B.empty_qtensor(N, K, device=dev)
+    B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE, out=nqx)
+    B.nvfp4_quantize(w, B.NVFP4_Q_2D, out=nqw)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    amax = torch.zeros(3, dtype=torch.float32, device=dev)
+    g_ms = time_ms_flushed(lambda: B.nvfp4_gemm(nqx, nqw, out=y, stream=stream), stream, flush)
+    ga_ms = time_ms_flushed(lambda: B.nvfp4_gemm_amax(nqx, nqw, out=y, amax=amax[:1], stream=stream), stream, flush)
+    a_ms = time_ms_flushed(lambda: B.nvfp4_amax(y, B.NVFP4_AMAX_PLAIN, out=amax, stream=stream), stream, flush)
+    if B.nvfp4_get_status() != B.NVFP4_OK:
+        raise RuntimeError("device status in the amax-epilogue measurement")
+    print(json.dumps({
+        "next": "amax_epilogue", "workload": "fprop_gemm_%dx%dx%d_bf16_out" % (M, K, N),
+        "gemm_ms": g_ms, "gemm_amax_ms": ga_ms, "separate_amax_pass_ms": a_ms,
+        "saved_ms": g_ms + a_ms - ga_ms, "note": "each launch alone, L2 flushed before it"}), flush=True)
+
+    # (2) NEXT-3: the MXFP4 layer step
     qx, qxt = B.empty_mx_qtensor(M, K, device=dev), B.empty_mx_qtensor(K, M, device=dev)
     qw, qwt = B.empty_mx_qtensor(N, K, device=dev), B.empty_mx_qtensor(K, N, device=dev)
     qdy, qdyt = B.empty_mx_qtensor(M, N, device=dev), B.empty_mx_qtensor(N, M, device=dev)
@@ -555,23 +572,18 @@ def run_mx(args, rank, world, local):
     step()
     launches = B.nvfp4_kernel_launch_count() - n0
     ms = time_ms(step, stream, reps=args.steps, warm=args.warmup)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     part_ms = {k: time_ms_flushed(f, stream, flush) for k, f in parts.items()}
     if B.nvfp4_get_status() != B.NVFP4_OK:
         raise RuntimeError("device status in the MXFP4 step")
     # NVFP4 GEMM of the same Fprop shape (operands from the NVFP4 quantizers)
-    nqx = B.empty_qtensor(M, K, device=dev)
-    nqw = B.empty_qtensor(N, K, device=dev)
-    B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE, out=nqx)
-    B.nvfp4_quantize(w, B.NVFP4_Q_2D, out=nqw)
-    nv_ms = time_ms_flushed(lambda: B.nvfp4_gemm(nqx, nqw, out=y, stream=stream), stream, flush)
+    nv_ms = g_ms
     # algorithmic bytes of one fused MXFP4 quantization of an [r, c] tensor:
     # read 2 B, write two outputs of 0.5 B codes + 1/16 B scale words
     qbytes = lambda r, c: r * c * (2.0 + 2 * (0.5 + 1.0 / 16))  # noqa: E731
     dy_gbs = qbytes(M, N) / (part_ms["quant_dy"] * 1e-3) / 1e9
     gemm_tf = FLOPS_PER_GEMM / (part_ms["gemm_fprop"] * 1e-3) / 1e12
     print(json.dumps({
-        "mx": "layer", "workload": "mxfp4_linear_fwd_bwd_mlp_up_%dx%dx%d" % (M, K, N),
+        "next": "mxfp4_layer", "workload": "mxfp4_linear_fwd_bwd_mlp_up_%dx%dx%d" % (M, K, N),
         "ms_per_step": ms, "value": FLOPS_PER_STEP / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
         "gpu_launches_per_step": launches, "parts_ms_l2_flushed": part_ms,
         "roofline_quant_dy": {"bound": "hbm", "achieved": dy_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -580,6 +592,21 @@ def run_mx(args, rank, world, local):
                                 "frac": gemm_tf / fp4_peak, "peak_source": src + " bf16 x 6 (nominal fp4:bf16)"},
         "nvfp4_gemm_fprop_ms_l2_flushed": nv_ms,
     }), flush=True)
+    del qx, qxt, qw, qwt, qdy, qdyt, nqx, nqw
+
+    # (3) NEXT-4: a layer kept in BF16 (cuBLAS GEMMs inside the library)
+    def bf16_step():
+        B.nvfp4_linear_bf16_fwd(x, w, y=y, stream=stream)
+        B.nvfp4_linear_bf16_bwd(dy, x, w, dx=dx, dw=dw, stream=stream)
+
+    bms = time_ms(bf16_step, stream, reps=args.steps, warm=args.warmup)
+    btf = FLOPS_PER_STEP / (bms * 1e-3) / 1e12
+    print(json.dumps({
+        "next": "bf16_layer", "workload": "bf16_linear_fwd_bwd_mlp_up_%dx%dx%d" % (M, K, N),
+        "ms_per_step": bms, "value": btf, "unit": "TFLOP/s",
+        "roofline": {"bound": "tensor", "achieved": btf, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": btf / bf16_peak, "peak_source": src + " bf16 burst"},
+        "gemms": "cuBLAS (cublasGemmEx, BF16, FP32 accumulation)"}), flush=True)
     return 0
 
 
@@ -591,8 +618,9 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line, one line per further configured shape")
-    ap.add_argument("--mx", action="store_true",
-                    help="instead of the benchmark line, the MXFP4 variant of the layer step")
+    ap.add_argument("--next", action="store_true",
+                    help="instead of the benchmark line, the further paths: GEMM-epilogue amax, the MXFP4 "
+                         "layer step, a BF16 layer step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gpu":
         args.warmup = 3
@@ -601,8 +629,8 @@ def main():
         return run_reference(args, rank, world)
     if args.sweep:
         return run_sweep(args, rank, world, local)
-    if args.mx:
-        return run_mx(args, rank, world, local)
+    if args.next:
+        return run_next(args, rank, world, local)
     return run_gpu(args, rank, world, local)
 
 

@@ -334,6 +334,27 @@ nvfp4_status nvfp4_linear_fwd_noalloc(const void* x_dev, const void* w_dev, int6
                                       uint64_t seed, void* y_dev, nvfp4_stream stream);
 
 /*
+ * The linear layers the method keeps in BF16 (Resumo técnico §2, item 1,
+ * "Precisão Mista Seletiva": the sensitive layers -- the last ones of the
+ * network, about 15% -- stay in BF16 while the rest trains in NVFP4): the
+ * same layer step without quantization, BF16 in and out, FP32 accumulation,
+ * on cuBLAS.
+ *   nvfp4_linear_bf16_fwd: Y = X W^T.
+ *   nvfp4_linear_bf16_bwd: dX = dY W and dW = dY^T X.
+ *   x_dev [M, K], w_dev [N, K], dy_dev [M, N], y_dev [M, N], dx_dev [M, K],
+ *   dw_dev [N, K]: BF16, row-major, contiguous.
+ * Sizes: M, K, N positive, K and N multiples of 8 (16-byte rows).
+ * Streams: enqueued on `stream`.  The first call on a device creates the
+ * library's cuBLAS handle for it (cuBLAS allocates its own workspace then);
+ * make it outside stream capture.  Calls from several host threads are
+ * serialised while they enqueue.  A cuBLAS failure returns NVFP4_ERR_CUDA.
+ */
+nvfp4_status nvfp4_linear_bf16_fwd(const void* x_dev, const void* w_dev, int64_t M, int64_t K, int64_t N,
+                                   void* y_dev, nvfp4_stream stream);
+nvfp4_status nvfp4_linear_bf16_bwd(const void* dy_dev, const void* x_dev, const void* w_dev, int64_t M,
+                                   int64_t K, int64_t N, void* dx_dev, void* dw_dev, nvfp4_stream stream);
+
+/*
  * nvfp4_get_status -- synchronises `stream`, then returns and clears the
  * current device's status word (NVFP4_OK if no device-side error was seen
  * since the last call); NVFP4_ERR_CUDA if the synchronisation failed.

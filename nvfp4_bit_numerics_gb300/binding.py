@@ -46,6 +46,7 @@ EXPORTED = [
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_linear_get_views", "nvfp4_get_status",
     "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
     "nvfp4_debug_stall_next_gemm", "nvfp4_gemm_amax", "nvfp4_quantize_mx", "nvfp4_mx_scale_bytes",
+    "nvfp4_linear_bf16_fwd", "nvfp4_linear_bf16_bwd",
 ]
 
 
@@ -101,6 +102,8 @@ def load_library(path=LIB_PATH):
         "nvfp4_debug_stall_next_gemm": (None, [I32]),
         "nvfp4_quantize_mx": (I32, [P, I64, I64, I32, T, T, P]),
         "nvfp4_mx_scale_bytes": (SZ, [I64, I64, I32]),
+        "nvfp4_linear_bf16_fwd": (I32, [P, P, I64, I64, I64, P, P]),
+        "nvfp4_linear_bf16_bwd": (I32, [P, P, P, I64, I64, I64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -287,6 +290,38 @@ def nvfp4_linear_fwd_noalloc(x, w, seed, y=None, stream=None):
     _check("nvfp4_linear_fwd_noalloc", load_library().nvfp4_linear_fwd_noalloc(
         _ptr(x), _ptr(w), M, K, N, seed, _ptr(y), _stream(stream)))
     return y
+
+
+def nvfp4_linear_bf16_fwd(x, w, y=None, stream=None):
+    """Y = X W^T for a layer kept in BF16 (cuBLAS inside the library)."""
+    _bf16_2d(x, "x")
+    _bf16_2d(w, "w")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("w must be [N, %d]" % K)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check("nvfp4_linear_bf16_fwd", load_library().nvfp4_linear_bf16_fwd(_ptr(x), _ptr(w), M, K, N, _ptr(y),
+                                                                         _stream(stream)))
+    return y
+
+
+def nvfp4_linear_bf16_bwd(dy, x, w, dx=None, dw=None, stream=None):
+    """dX = dY W and dW = dY^T X for a layer kept in BF16; returns (dx, dw)."""
+    for t, n in ((dy, "dy"), (x, "x"), (w, "w")):
+        _bf16_2d(t, n)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or tuple(dy.shape) != (M, N):
+        raise ValueError("shapes must be dy [M, N], x [M, K], w [N, K]")
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    if dw is None:
+        dw = torch.empty((N, K), dtype=torch.bfloat16, device=x.device)
+    _check("nvfp4_linear_bf16_bwd", load_library().nvfp4_linear_bf16_bwd(
+        _ptr(dy), _ptr(x), _ptr(w), M, K, N, _ptr(dx), _ptr(dw), _stream(stream)))
+    return dx, dw
 
 
 def nvfp4_linear_get_views(ws, M, K, N):

@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4.so")
-SOURCES = ["api.cu", "quant_kernels.cu", "mx_kernels.cu", "gemm_kernel.cu", "static_workspace.cu"]
+SOURCES = ["api.cu", "quant_kernels.cu", "mx_kernels.cu", "gemm_kernel.cu", "bf16_linear.cu",
+           "static_workspace.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -61,7 +62,11 @@ def build(force=False, verbose=False):
             if err:
                 print(err, file=sys.stderr)
     tmp = LIB + ".tmp"
-    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results] + ["-cudart", "static"]
+    # cuBLAS serves the BF16 layers; the rpath finds the toolkit's copy when
+    # the loader's search path does not
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
+    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results] + \
+        ["-cudart", "static", "-lcublas", "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))

@@ -33,3 +33,13 @@ def gemm_ref(a_codes, a_scales, ts_a, b_codes, b_scales, ts_b, rows=None):
     A = dequant_operand(a_codes, a_scales, rows)
     B = dequant_operand(b_codes, b_scales)
     return (A @ B.T) * (np.float64(ts_a) * np.float64(ts_b))
+
+
+def linear_bf16_ref(x, w, dy):
+    """The layer step of a linear layer kept in BF16 (Resumo técnico §2,
+    item 1, "Precisão Mista Seletiva"): Y = X W^T, dX = dY W, dW = dY^T X for
+    X [M, K], W [N, K], dY [M, N] given as float arrays holding BF16 values.
+    Products of BF16 values are exact in float64; the sums are float64
+    matrix products.  Returns (Y, dX, dW) in float64."""
+    x, w, dy = (np.asarray(a, dtype=np.float64) for a in (x, w, dy))
+    return x @ w.T, dy @ w, dy.T @ x

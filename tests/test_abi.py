@@ -148,3 +148,14 @@ def test_linear_argument_checks(lib):
     assert f(w=None) == binding.NVFP4_ERR_ARG
     assert f(w=ctypes.c_void_p(8)) == binding.NVFP4_ERR_ALIGN
     assert lib.nvfp4_linear_bwd(p, 128, 256, 256, 1, p, None, p, ws, None) == binding.NVFP4_ERR_ARG
+    # BF16 layers (checked before cuBLAS is touched)
+    bf = lambda M=100, K=64, N=72, x=p, y=p: lib.nvfp4_linear_bf16_fwd(x, p, M, K, N, y, None)  # noqa: E731
+    assert bf(M=0) == binding.NVFP4_ERR_SHAPE
+    assert bf(K=60) == binding.NVFP4_ERR_SHAPE
+    assert bf(N=70) == binding.NVFP4_ERR_SHAPE
+    assert bf(x=None) == binding.NVFP4_ERR_ARG
+    assert bf(y=ctypes.c_void_p(24)) == binding.NVFP4_ERR_ALIGN
+    bb = lambda dx=p, K=64: lib.nvfp4_linear_bf16_bwd(p, p, p, 100, K, 72, dx, p, None)  # noqa: E731
+    assert bb(dx=None) == binding.NVFP4_ERR_ARG
+    assert bb(K=-8) == binding.NVFP4_ERR_SHAPE
+    assert bb(dx=ctypes.c_void_p(40)) == binding.NVFP4_ERR_ALIGN

@@ -96,3 +96,40 @@ def test_workload_generator_is_deterministic():
     x = workloads.bf16_to_f32_numpy(a[0])
     big_cols = np.flatnonzero(np.abs(x).max(axis=0) > 20)
     assert len(big_cols) == 2
+
+
+def test_linear_bf16_closed_form_and_one_hot_orientation():
+    """The BF16 layer step: constant operands give K, N and M times the
+    products; one-hot inputs pin which operand is transposed in each of the
+    three products."""
+    M, K, N = 3, 4, 5
+    y, dx, dw = gemm.linear_bf16_ref(np.full((M, K), 0.5), np.full((N, K), 3.0), np.full((M, N), -2.0))
+    np.testing.assert_array_equal(y, np.full((M, N), K * 1.5))
+    np.testing.assert_array_equal(dx, np.full((M, K), N * -6.0))
+    np.testing.assert_array_equal(dw, np.full((N, K), M * -1.0))
+    x = np.zeros((M, K)); x[2, 1] = 2.0
+    w = np.zeros((N, K)); w[4, 1] = 3.0
+    dy = np.zeros((M, N)); dy[2, 4] = 5.0
+    y, dx, dw = gemm.linear_bf16_ref(x, w, dy)
+    assert np.argwhere(y).tolist() == [[2, 4]] and y[2, 4] == 6.0
+    assert np.argwhere(dx).tolist() == [[2, 1]] and dx[2, 1] == 15.0   # row 2 of dY picks row 4 of W
+    assert np.argwhere(dw).tolist() == [[4, 1]] and dw[4, 1] == 10.0   # dY^T X: column 4 of dY, row 2 of X
+
+
+def test_linear_bf16_matches_loop_brute_force():
+    """Element-by-element sums in exact rationals on small random BF16
+    operands (independent of the matrix-product routine)."""
+    rng = np.random.default_rng(7)
+    M, K, N = 3, 5, 4
+    bf = lambda a: workloads.bf16_to_f32_numpy(workloads.to_bf16(a.astype(np.float32)))  # noqa: E731
+    x, w, dy = bf(rng.standard_normal((M, K))), bf(rng.standard_normal((N, K))), bf(rng.standard_normal((M, N)))
+    y, dx, dw = gemm.linear_bf16_ref(x, w, dy)
+    F = lambda v: Fraction(float(v))  # noqa: E731
+    for i in range(M):
+        for j in range(N):
+            assert Fraction(y[i, j]) == sum(F(x[i, k]) * F(w[j, k]) for k in range(K))
+        for k in range(K):
+            assert Fraction(dx[i, k]) == sum(F(dy[i, j]) * F(w[j, k]) for j in range(N))
+    for j in range(N):
+        for k in range(K):
+            assert Fraction(dw[j, k]) == sum(F(dy[i, j]) * F(x[i, k]) for i in range(M))
