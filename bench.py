@@ -513,8 +513,10 @@ def time_ms_flushed(fn, stream, flush, reps=5, warm=2):
 def run_next(args, rank, world, local):
     """--next: one JSON line per further path built on the same workload:
     (1) the GEMM epilogue's output amax (nvfp4_gemm_amax) against the plain
-    GEMM plus a separate amax pass over its output; (2) the MXFP4 variant of
-    the layer step; (3) the layer step of a layer kept in BF16."""
+    GEMM plus a separate amax pass over its output; (2) the output quantized
+    in the epilogue (nvfp4_gemm_quant) against the GEMM plus a separate
+    quantize; (3) the MXFP4 variant of the layer step; (4) the layer step of
+    a layer kept in BF16."""
     import torch
 
     from nvfp4_bit_numerics_gb300 import binding as B, build as nbuild, workloads
@@ -546,6 +548,23 @@ def run_next(args, rank, world, local):
         "next": "amax_epilogue", "workload": "fprop_gemm_%dx%dx%d_bf16_out" % (M, K, N),
         "gemm_ms": g_ms, "gemm_amax_ms": ga_ms, "separate_amax_pass_ms": a_ms,
         "saved_ms": g_ms + a_ms - ga_ms, "note": "each launch alone, L2 flushed before it"}), flush=True)
+
+    # NEXT-2: Y quantized for the next layer in the GEMM epilogue (amax of the
+    # previous, identical step) against the GEMM plus a separate quantize of Y
+    yq = B.empty_qtensor(M, N, device=dev)
+    yq.amax.copy_(amax[:1])
+    q_ms = time_ms_flushed(lambda: B.nvfp4_quantize(y, B.NVFP4_Q_ROWWISE, compute_amax=False, out=yq,
+                                                    stream=stream), stream, flush)
+    gq_ms = time_ms_flushed(lambda: B.nvfp4_gemm_quant(nqx, nqw, yq, stream=stream), stream, flush)
+    gqy_ms = time_ms_flushed(lambda: B.nvfp4_gemm_quant(nqx, nqw, yq, out=y, stream=stream), stream, flush)
+    if B.nvfp4_get_status() != B.NVFP4_OK:
+        raise RuntimeError("device status in the quantize-in-epilogue measurement")
+    print(json.dumps({
+        "next": "quantize_epilogue", "workload": "fprop_gemm_%dx%dx%d_nvfp4_out" % (M, K, N),
+        "gemm_bf16_ms": g_ms, "separate_quantize_of_y_ms": q_ms, "gemm_quant_ms": gq_ms,
+        "gemm_quant_plus_bf16_ms": gqy_ms, "saved_ms": g_ms + q_ms - gq_ms,
+        "note": "each launch alone, L2 flushed before it; gemm_quant writes only the NVFP4 Y"}), flush=True)
+    del yq
 
     # (2) NEXT-3: the MXFP4 layer step
     qx, qxt = B.empty_mx_qtensor(M, K, device=dev), B.empty_mx_qtensor(K, M, device=dev)

@@ -261,6 +261,27 @@ nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* a, const nvfp4_tensor* b, void*
                              int64_t ldd, float* amax_dev, nvfp4_stream stream);
 
 /*
+ * nvfp4_gemm_quant -- nvfp4_gemm whose epilogue also writes its output
+ * already quantized for the next layer's Fprop: D is rounded to BF16 and each
+ * row's 1x16 blocks are quantized to NVFP4 with round-to-nearest-even, exactly
+ * as nvfp4_quantize(ROWWISE, RNE, no transform, compute_amax = 0) of that BF16
+ * D would quantize it, so the BF16 D need not be written and read back.  The
+ * pages fix no policy for the tensor amax of a tensor quantized where it is
+ * produced; the caller supplies it (for instance the previous step's
+ * nvfp4_gemm_amax of the same layer, a delayed amax).
+ *   y_q       [M, N] NVFP4, NVFP4_SCALES_MMA; its amax (device, 1 float) is
+ *             read; its codes, scales and tensor_scale are written.  A
+ *             non-finite amax sets NVFP4_ERR_NONFINITE in the status word.
+ *   d_dev     BF16 [M, ldd] output as in nvfp4_gemm, or NULL for none.
+ *   amax_dev  NULL, or one float that receives max |D| (as nvfp4_gemm_amax);
+ *             must not be y_q->amax.
+ * Operands: NVFP4 (not MXFP4).  Sizes: M % 256 == 0, N % 256 == 0 (the
+ * CTA-pair kernel), K % 64 == 0; other rules as nvfp4_gemm.
+ */
+nvfp4_status nvfp4_gemm_quant(const nvfp4_tensor* a, const nvfp4_tensor* b, const nvfp4_tensor* y_q,
+                              void* d_dev, int64_t ldd, float* amax_dev, nvfp4_stream stream);
+
+/*
  * One NVFP4 linear layer Y = X W^T, X [M, K] tokens x in-features, W [N, K].
  *
  * nvfp4_linear_fwd: amax of X, of the Hadamard-transformed X^T and of W;

@@ -46,7 +46,7 @@ EXPORTED = [
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_linear_get_views", "nvfp4_get_status",
     "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
     "nvfp4_debug_stall_next_gemm", "nvfp4_gemm_amax", "nvfp4_quantize_mx", "nvfp4_mx_scale_bytes",
-    "nvfp4_linear_bf16_fwd", "nvfp4_linear_bf16_bwd",
+    "nvfp4_linear_bf16_fwd", "nvfp4_linear_bf16_bwd", "nvfp4_gemm_quant",
 ]
 
 
@@ -91,6 +91,7 @@ def load_library(path=LIB_PATH):
         "nvfp4_scale_bytes": (SZ, [I64, I64, I32]),
         "nvfp4_gemm": (I32, [T, T, P, I32, I64, P]),
         "nvfp4_gemm_amax": (I32, [T, T, P, I32, I64, P, P]),
+        "nvfp4_gemm_quant": (I32, [T, T, T, P, I64, P, P]),
         "nvfp4_linear_workspace_bytes": (SZ, [I64, I64, I64]),
         "nvfp4_linear_fwd": (I32, [P, P, I64, I64, I64, U64, P, P, SZ, P]),
         "nvfp4_linear_bwd": (I32, [P, I64, I64, I64, U64, P, P, P, SZ, P]),
@@ -244,6 +245,18 @@ def nvfp4_gemm_amax(a, b, out=None, out_dtype=torch.bfloat16, amax=None, stream=
     _check("nvfp4_gemm_amax", load_library().nvfp4_gemm_amax(ctypes.byref(sa), ctypes.byref(sb), _ptr(out), dt,
                                                              out.stride(0), _ptr(amax), _stream(stream)))
     return out, amax
+
+
+def nvfp4_gemm_quant(a, b, yq, out=None, amax_out=None, stream=None):
+    """D = A B^T with D also written NVFP4-quantized into the QTensor yq
+    (whose amax the caller has set); out: optional BF16 [M, N] output;
+    amax_out: optional one-float tensor receiving max |D|.  Returns
+    (yq, out, amax_out)."""
+    sa, sb, sq = a.struct(), b.struct(), yq.struct()
+    ldd = out.stride(0) if out is not None else b.rows
+    _check("nvfp4_gemm_quant", load_library().nvfp4_gemm_quant(
+        ctypes.byref(sa), ctypes.byref(sb), ctypes.byref(sq), _ptr(out), ldd, _ptr(amax_out), _stream(stream)))
+    return yq, out, amax_out
 
 
 def nvfp4_linear_workspace_bytes(M, K, N):

@@ -288,6 +288,23 @@ nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* a, const nvfp4_tensor* b, void*
   return launch_gemm(*a, *b, d, d_dtype, ldd, s, amax_dev);
 }
 
+nvfp4_status nvfp4_gemm_quant(const nvfp4_tensor* a, const nvfp4_tensor* b, const nvfp4_tensor* y_q, void* d,
+                              int64_t ldd, float* amax_dev, nvfp4_stream stream) {
+  if (!y_q || !valid_tensor(y_q) || !y_q->amax || y_q->format != NVFP4_FORMAT_NVFP4) return NVFP4_ERR_ARG;
+  if (y_q->scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_ARG;
+  if (amax_dev && amax_dev == y_q->amax) return NVFP4_ERR_ARG;  // the output amax would clear the input one
+  // the GEMM checks, with the code buffer standing in for an absent BF16 output
+  const nvfp4_status st = check_gemm(a, b, d ? d : y_q->codes, NVFP4_OUT_BF16, d ? ldd : b->rows);
+  if (st != NVFP4_OK) return st;
+  if (a->format != NVFP4_FORMAT_NVFP4) return NVFP4_ERR_ARG;
+  if (a->rows % 256 || b->rows % 256) return NVFP4_ERR_SHAPE;
+  if (y_q->rows != a->rows || y_q->cols != b->rows) return NVFP4_ERR_SHAPE;
+  if (amax_dev && (reinterpret_cast<uintptr_t>(amax_dev) & 3u) != 0) return NVFP4_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (amax_dev && cudaMemsetAsync(amax_dev, 0, sizeof(float), s) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return launch_gemm(*a, *b, d, NVFP4_OUT_BF16, ldd, s, amax_dev, y_q);
+}
+
 // ---------------------------------------------------------------------------
 // Linear layer
 // ---------------------------------------------------------------------------

@@ -304,6 +304,23 @@ __device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, const f
   return out;
 }
 
+// The same block with round-to-nearest-even and enc computed by its division
+// (the value fill_enc_table stores), for kernels without a table.
+__device__ __forceinline__ uint2 quantize16_rne(const float* v, float s_enc, uint32_t& E) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  float enc;
+  block_scale(m, s_enc, E, enc);
+  float s[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s[i] = __fmul_rn(v[i], enc);
+  uint2 out;
+  out.x = e2m1x8_rn(s);
+  out.y = e2m1x8_rn(s + 8);
+  return out;
+}
+
 // Byte offset of scale (row r, block kb) in the MMA scale layout of a tensor
 // with n_kb = cols/16 blocks per row (n_kb % 4 == 0): 512-byte tiles of 128
 // rows x 4 blocks, row-tile major; (r%32)*16 + ((r/32)%4)*4 + kb%4 inside.

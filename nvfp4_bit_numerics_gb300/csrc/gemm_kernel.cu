@@ -101,6 +101,12 @@ struct Params {
   int tma_store;   // pair kernel: BF16 output written by bulk tensor stores
   uint32_t* amax_out;  // if set: max |D| over the stored output, as float bits (atomicMax)
   int mx;              // operands are MXFP4 (UE8M0 scales per 32, no tensor scales)
+  // pair kernel: the BF16 output quantized to NVFP4 (1x16, RNE) in the
+  // epilogue, with the tensor amax given by the caller (q_codes != nullptr)
+  uint8_t* q_codes;
+  uint8_t* q_scales;
+  const float* q_amax;
+  float* q_ts;
   uint32_t* status;
 };
 
@@ -819,6 +825,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const int half = (warp - kFirstEpiWarp) >> 2;
     constexpr int kCols = kPairBN / 2;
     const float alpha = p.mx ? 1.0f : __fmul_rn(*p.ts_a, *p.ts_b);
+    float q_senc = 1.0f;  // quantized output: the encode scale of its tensor amax
+    if (p.q_codes) {
+      const float a = *p.q_amax;
+      q_senc = tensor_encode_scale(a);
+      if (blockIdx.x == 0 && warp == kFirstEpiWarp && lane == 0) {
+        *p.q_ts = tensor_decode_scale(q_senc);
+        if (!(abs_bits(a) < 0x7F800000u)) raise_status(p.status, kStatusNonFinite);
+      }
+    }
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < n_tiles; tile += num_pairs) {
       int mb, nb;
@@ -882,9 +897,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           __syncwarp();
           if (lane == 0) tma_store_2d(&tmap_d, (int)col0 + 16 * j, (int)(row - lane), buf);
         }
-        if (p.amax_out) amax_bf16_words<kCols / 2>(packed, p.amax_out);
-      } else if (p.amax_out) {
-        amax_bits_to_global(m32, p.amax_out);
+      }
+      if (p.amax_out) {
+        if (!p.d_f32) amax_bf16_words<kCols / 2>(packed, p.amax_out);
+        else amax_bits_to_global(m32, p.amax_out);
+      }
+      if (p.q_codes) {
+        // this lane's row, 128 columns = 8 blocks of 16 BF16 values, each
+        // quantized as the rowwise RNE quantizer would quantize the stored
+        // BF16 output: 64 code bytes and two 4-scale words
+        uint32_t sc[2] = {0u, 0u};
+        uint4* cdst = reinterpret_cast<uint4*>(p.q_codes + row * (p.N >> 1) + (col0 >> 1));
+#pragma unroll
+        for (int b = 0; b < kCols / 16; b += 2) {
+          uint2 o[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              v[2 * i] = bf16lo(packed[8 * (b + h) + i]);
+              v[2 * i + 1] = bf16hi(packed[8 * (b + h) + i]);
+            }
+            uint32_t E;
+            o[h] = quantize16_rne(v, q_senc, E);
+            sc[(b + h) >> 2] |= E << (8 * ((b + h) & 3));
+          }
+          cdst[b >> 1] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+        }
+        const int64_t n_kb = p.N >> 4, kb0 = col0 >> 4;
+        *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0, n_kb)) = sc[0];
+        *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0 + 4, n_kb)) = sc[1];
       }
     }
     // the output is in global memory (and the buffers free) before exit
@@ -972,6 +1015,10 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
   p.status = device_status_ptr();
   p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
   p.mx = a.format == NVFP4_FORMAT_MXFP4;
+  p.q_codes = nullptr;
+  p.q_scales = nullptr;
+  p.q_amax = nullptr;
+  p.q_ts = nullptr;
   p.tma_store = 0;
   const int tiles = (p.M / kBM) * (p.N / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
@@ -982,7 +1029,7 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
 
 
 nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                      float* amax_out, cudaStream_t s) {
+                      float* amax_out, const nvfp4_tensor* yq, cudaStream_t s) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1014,10 +1061,15 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   p.status = device_status_ptr();
   p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
   p.mx = a.format == NVFP4_FORMAT_MXFP4;
+  p.q_codes = yq ? yq->codes : nullptr;
+  p.q_scales = yq ? yq->scales : nullptr;
+  p.q_amax = yq ? yq->amax : nullptr;
+  p.q_ts = yq ? yq->tensor_scale : nullptr;
   // BF16 output goes through bulk tensor stores (the API guarantees the
-  // 16-byte aligned base and row stride they need); FP32 through plain stores
-  CUtensorMap md = ma;  // unused for FP32 output
-  p.tma_store = !p.d_f32;
+  // 16-byte aligned base and row stride they need); FP32 through plain
+  // stores; no BF16 output (quantized output only) stores nothing
+  CUtensorMap md = ma;  // unused for FP32 or no BF16 output
+  p.tma_store = !p.d_f32 && d != nullptr;
   if (p.tma_store && !make_out_map(&md, d, (uint64_t)p.N, (uint64_t)p.M, (uint64_t)ldd)) return NVFP4_ERR_CUDA;
   const int tiles = (p.M / 256) * (p.N / kPairBN);
   const int pairs_max = sm_count() / 2;
@@ -1032,8 +1084,9 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
 void set_gemm_debug_stall(int on) { g_debug_stall.store(on ? 1 : 0); }
 
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                         cudaStream_t s, float* amax_out) {
-  if (a.rows % 256 == 0 && b.rows % 256 == 0) return run_pair(a, b, d, d_dtype, ldd, amax_out, s);
+                         cudaStream_t s, float* amax_out, const nvfp4_tensor* yq) {
+  if (a.rows % 256 == 0 && b.rows % 256 == 0) return run_pair(a, b, d, d_dtype, ldd, amax_out, yq, s);
+  if (yq) return NVFP4_ERR_SHAPE;  // the quantized output is produced by the CTA-pair kernel only
   if (b.rows % 256 == 0) return run<256>(a, b, d, d_dtype, ldd, amax_out, s);
   return run<128>(a, b, d, d_dtype, ldd, amax_out, s);
 }

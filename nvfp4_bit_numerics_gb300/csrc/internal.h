@@ -63,8 +63,11 @@ void set_gemm_debug_stall(int on);
 
 // GEMM launcher (gemm_kernel.cu).  Arguments are already validated.  With
 // amax_out set (a zeroed device float), the epilogue also takes the max |D|
-// over the stored output into it.
+// over the BF16 (or FP32) output into it.  With yq set (BF16 output, M and N
+// multiples of 256), the epilogue also quantizes the BF16 output into yq
+// (1x16 RNE, MMA scale layout, tensor amax read from yq->amax); d may then be
+// nullptr (no BF16 store).
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                         cudaStream_t s, float* amax_out = nullptr);
+                         cudaStream_t s, float* amax_out = nullptr, const nvfp4_tensor* yq = nullptr);
 
 }  // namespace nvfp4

@@ -90,6 +90,24 @@ def test_gemm_argument_checks(lib):
     assert call(_mx(128, 256, layout=0), _mx(256, 256)) == binding.NVFP4_ERR_ARG
 
 
+def test_gemm_quant_argument_checks(lib):
+    a, b = _t(256, 256), _t(512, 256)
+    yq = _t(256, 512, amax=32)
+    d = ctypes.c_void_p(16)
+    g = lambda a_=a, b_=b, y_=yq, d_=d, amax_=None: lib.nvfp4_gemm_quant(  # noqa: E731
+        ctypes.byref(a_), ctypes.byref(b_), ctypes.byref(y_) if y_ is not None else None, d_, 512, amax_, None)
+    assert g(y_=None) == binding.NVFP4_ERR_ARG
+    assert g(y_=_t(256, 512, amax=None)) == binding.NVFP4_ERR_ARG         # the amax is an input
+    assert g(y_=_t(256, 512, layout=0)) == binding.NVFP4_ERR_ARG          # MMA scale layout only
+    assert g(y_=_t(256, 512, fmt=binding.NVFP4_FORMAT_MXFP4)) == binding.NVFP4_ERR_ARG
+    assert g(amax_=ctypes.c_void_p(32)) == binding.NVFP4_ERR_ARG          # same slot as y_q->amax
+    assert g(a_=_t(128, 256), y_=_t(128, 512)) == binding.NVFP4_ERR_SHAPE  # pair kernel: M % 256
+    assert g(y_=_t(256, 256)) == binding.NVFP4_ERR_SHAPE
+    assert g(a_=_mx(256, 256), b_=_mx(512, 256)) == binding.NVFP4_ERR_ARG
+    assert g(amax_=ctypes.c_void_p(18)) == binding.NVFP4_ERR_ALIGN
+    assert g(d_=ctypes.c_void_p(24)) == binding.NVFP4_ERR_ALIGN
+
+
 def test_quantize_mx_argument_checks(lib):
     x = ctypes.c_void_p(16)
     out, out_t = _mx(128, 256), _mx(256, 128)
