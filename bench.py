@@ -436,10 +436,77 @@ def run_gpu(args, rank, world, local):
     return 0
 
 
+def run_quant_sweep(stream, dev):
+    """The quantize-only sweep (two BF16 tensors, 8192x5120 and 8192x20480,
+    N(0,1) with 0.1 % heavy-tailed entries): each amax pass and each
+    quantize mode alone -- the tensor amax already computed, as in the layer
+    step -- with the L2 flushed before every launch.  Algorithmic bytes: an
+    amax pass reads 2 B per element; a quantize reads 2 B and writes 0.5 B of
+    codes and 1/16 B of scales per element for each output."""
+    import torch
+
+    from nvfp4_bit_numerics_gb300 import binding as B, workloads
+
+    hbm_peak, _, src = measured_peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    seed = 2024
+    for x_h in workloads.quant_sweep():
+        x = x_h.to(dev)
+        rows, cols = x.shape
+        n = rows * cols
+        amax = torch.zeros(3, dtype=torch.float32, device=dev)
+        out = B.empty_qtensor(rows, cols, device=dev)
+        out_t = B.empty_qtensor(cols, rows, device=dev)
+        B.nvfp4_amax(x, 7, rht_seed=seed, out=amax)  # plain, Hadamard along rows, Hadamard along columns
+        torch.cuda.synchronize()
+
+        def q(kind, rounding, rht, a_row, a_t=None):
+            """A quantize call whose outputs' amaxes (slots of `amax`) are set
+            before it is timed."""
+            def f():
+                first = out_t if kind == B.NVFP4_Q_TRANSPOSE else out
+                B.nvfp4_quantize(x, kind, rounding, rht=rht, seed=seed, sr_stream=0, sr_stream_t=1,
+                                 compute_amax=False, out=first,
+                                 out_t=out_t if kind in (B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, B.NVFP4_Q_2D) else None,
+                                 stream=stream)
+            f.amax_slots = (a_row, a_t)
+            return f
+
+        RNE, SR = B.NVFP4_ROUND_RNE, B.NVFP4_ROUND_SR
+        modes = [
+            ("amax_plain", lambda: B.nvfp4_amax(x, B.NVFP4_AMAX_PLAIN, out=amax, stream=stream), 2.0),
+            ("amax_plain_and_rht_cols", lambda: B.nvfp4_amax(x, B.NVFP4_AMAX_PLAIN | B.NVFP4_AMAX_RHT_COLS,
+                                                             rht_seed=seed, out=amax, stream=stream), 2.0),
+            ("rowwise_1x16_rne", q(B.NVFP4_Q_ROWWISE, RNE, False, 0), 2.5625),
+            ("rowwise_1x16_sr", q(B.NVFP4_Q_ROWWISE, SR, False, 0), 2.5625),
+            ("rowwise_1x16_rht_rne", q(B.NVFP4_Q_ROWWISE, RNE, True, 1), 2.5625),
+            ("2d_16x16_rne_w_and_wt", q(B.NVFP4_Q_2D, RNE, False, 0), 3.125),
+            ("transpose_1x16_rht_rne", q(B.NVFP4_Q_TRANSPOSE, RNE, True, None, 2), 2.5625),
+            ("transpose_1x16_rht_sr", q(B.NVFP4_Q_TRANSPOSE, SR, True, None, 2), 2.5625),
+            ("fused_rowwise_rne_and_transpose_rht_rne", q(B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, RNE, True, 0, 2), 3.125),
+            ("fused_rowwise_sr_and_transpose_rht_sr", q(B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, SR, True, 0, 2), 3.125),
+        ]
+        for name, fn, bpe in modes:
+            a_row, a_t = getattr(fn, "amax_slots", (None, None))
+            if a_row is not None:
+                out.amax.copy_(amax[a_row:a_row + 1])
+            if a_t is not None:
+                out_t.amax.copy_(amax[a_t:a_t + 1])
+            ms = time_ms_flushed(fn, stream, flush)
+            gbs = n * bpe / (ms * 1e-3) / 1e9
+            print(json.dumps({"sweep": "quantize", "workload": "%s_%dx%d" % (name, rows, cols), "ms": ms,
+                              "value": gbs, "unit": "GB/s", "frac_hbm": gbs / hbm_peak,
+                              "peak": hbm_peak, "peak_source": src, "bytes_per_element": bpe}), flush=True)
+        if B.nvfp4_get_status() != B.NVFP4_OK:
+            raise RuntimeError("device status in the quantize sweep")
+        del x, out, out_t
+
+
 def run_sweep(args, rank, world, local):
-    """--sweep: one JSON line per further configured shape (the layer step
-    for the MLP down-projection and the QKV projection; the GEMM alone for
-    the M = 16384 shape sweep), with the library GEMMs for context."""
+    """--sweep: one JSON line per further configured shape (the quantize-only
+    sweep; the layer step for the MLP down-projection and the QKV projection;
+    the GEMM alone for the M = 16384 shape sweep), with the library GEMMs for
+    context."""
     import torch
 
     from nvfp4_bit_numerics_gb300 import binding as B, build as nbuild, workloads
@@ -451,6 +518,7 @@ def run_sweep(args, rank, world, local):
     B.load_library()
     stream = torch.cuda.current_stream(dev)
     fp4_peak = measured_peaks()[1] * FP4_OVER_BF16
+    run_quant_sweep(stream, dev)
     for name, gen, (m, k, n) in [("mlp_down", workloads.mlp_down, (8192, 20480, 5120)),
                                  ("qkv", workloads.qkv, (8192, 5120, 7168))]:
         x, w, dy = (t.to(dev) for t in gen())
@@ -492,15 +560,19 @@ def run_sweep(args, rank, world, local):
 
 
 def time_ms_flushed(fn, stream, flush, reps=5, warm=2):
-    """Mean device time of fn() alone on `stream`, the L2 flushed (a write
-    of `flush`, larger than L2) before every launch."""
+    """Mean device time of fn() alone on `stream`, the L2 flushed before
+    every launch: a write of the first half of `flush` (larger than L2), then
+    a read of the second half, so that the write's dirty lines are written
+    back before the timed launch rather than during it."""
     import torch
 
+    half = flush.numel() // 2
     for _ in range(warm):
         fn()
     total = 0.0
     for _ in range(reps):
-        flush.add_(1)
+        flush[:half].add_(1)
+        flush[half:].max()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         fn()
@@ -530,7 +602,7 @@ def run_next(args, rank, world, local):
     hbm_peak, bf16_peak, src = measured_peaks()
     fp4_peak = bf16_peak * FP4_OVER_BF16
     x, w, dy = (t.to(dev) for t in workloads.mlp_up())
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
     # (1) NEXT-1: the output amax taken in the GEMM epilogue
     nqx = B.empty_qtensor(M, K, device=dev)

@@ -20,34 +20,21 @@
 //
 // The kernel is bound by HBM bandwidth: 2 bytes read per element, 0.5 + 1/16
 // bytes written per element and output (codes and MMA-layout scale words).
-// It is a persistent TMA pipeline: a producer warp streams 128 x 64 BF16
-// tiles (16 KB, 128-byte swizzle) into a 4-slot shared-memory ring with
-// cp.async.bulk.tensor, and 8 consumer warps encode each tile once it has
-// landed -- threads 0-127 one 64-element row chunk each (rowwise output),
-// threads 128-255 one 64-row column chunk each (transposed output) -- so
-// every thread writes whole 32-byte code runs and one whole scale word while
-// the next tiles are already in flight.  The swizzle (16-byte chunk j of row
-// r stored at chunk j ^ (r % 8)) makes both the row reads (8 rows per
-// 16-byte load phase) and the column reads (32 columns of one row) free of
-// shared-memory bank conflicts.
+// It runs on the TMA tile ring of tile_ring.cuh (128 x 64 BF16 tiles in a
+// 4-slot shared-memory ring): threads 0-127 encode one 64-element row chunk
+// each (rowwise output), threads 128-255 a column pair over 32 rows each
+// (transposed output), so every thread writes whole code runs and scale
+// words while the next tiles are already in flight.
 #include <cuda_runtime.h>
 
-#include "device_async.cuh"
 #include "device_common.cuh"
 #include "internal.h"
+#include "tile_ring.cuh"
 
 namespace nvfp4 {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
-constexpr int kRowsPerTile = 128;
-constexpr int kColsPerTile = 64;
-constexpr int kTileBytes = kRowsPerTile * kColsPerTile * 2;
-constexpr int kStages = 4;
-constexpr int kSmemBytes = kStages * kTileBytes + 1024;  // + alignment of the ring to 1024 B
 constexpr int kCtasPerSm = 3;
-constexpr int64_t kMaxTiles = int64_t(1) << 31;
 
 struct MxOut {
   uint8_t* codes;
@@ -111,7 +98,7 @@ __device__ __forceinline__ void mx_store_scales(const MxOut& o, int64_t r, int64
 // row r.
 __device__ __forceinline__ void row_offsets(int r, uint32_t* off) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) off[j] = (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4));
+  for (int j = 0; j < 8; ++j) off[j] = ring_chunk(r, j);
 }
 
 // Transposed thread u (0..127): the column pair (2 cp, 2 cp + 1) over the 32
@@ -137,18 +124,6 @@ __device__ __forceinline__ ColRole col_role(int u, uint32_t* off) {
     off[k] = (uint32_t)((32 * c.rb + ko) * 128 + (((cq ^ ko) & 7) << 4) + cw);
   }
   return c;
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
 }
 
 // Eight BF16 values (the low or high halves of eight words) -> one word of
@@ -227,87 +202,23 @@ __device__ __forceinline__ void encode_cols(uint32_t tile, const uint32_t* off, 
 }
 
 template <bool kRow, bool kT>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) mx_quant_kernel(const __grid_constant__ CUtensorMap xmap,
-                                                                        MxParams p) {
+__global__ void __launch_bounds__(kRingThreads, kCtasPerSm) mx_quant_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                            MxParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * kStages];  // full[s], empty[s]
-  __shared__ int abort_flag;
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t ring = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms are 1024 B
-  const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
-  volatile int* abort = &abort_flag;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  if (t == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumerWarps);
+  const int t = threadIdx.x;
+  // consumers: threads 0-127 rowwise, 128-255 transposed; their offsets
+  // into a tile are fixed for the whole kernel
+  uint32_t off[8];
+  ColRole col{};
+  if (t < 128) row_offsets(t, off);
+  else if (t < 256) col = col_role(t - 128, off);
+  tile_ring(&xmap, p.rows, p.cols, p.status, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
+    if (t < 128) {
+      if (kRow && t < valid) encode_row(tile, off, m0 + t, c0, p.cols, p.orow);
+    } else if (kT) {
+      if (64 * (col.rb >> 1) < valid) encode_cols(tile, off, col, m0, c0, p.rows, p.ot);  // warp-uniform
     }
-    abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-
-  const uint32_t tiles_c = (uint32_t)(p.cols / kColsPerTile);
-  const uint32_t n_tiles = (uint32_t)((p.rows + kRowsPerTile - 1) / kRowsPerTile) * tiles_c;  // < 2^31
-  if (warp == kConsumerWarps) {
-    // ---- producer: one lane streams this CTA's tiles into the ring ----
-    if (lane == 0) {
-      int n = 0;
-      for (uint32_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x, ++n) {
-        const int s = n % kStages;
-        if (n >= kStages && !mbar_wait(empty_bar(s), (uint32_t)((n / kStages) - 1) & 1u, abort, p.status)) break;
-        const uint32_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
-        mbar_arrive_expect_tx(full_bar(s), kTileBytes);
-        tma_load_2d(ring + (uint32_t)s * kTileBytes, &xmap, (int)(tc * kColsPerTile), (int)(tm * kRowsPerTile),
-                    full_bar(s));
-      }
-      // every load this CTA issued has landed before it exits: the last
-      // kStages loads' phases (the earlier ones were consumed), each wait
-      // bounded and independent of the abort flag
-      volatile int never = 0;
-      for (int k = n - kStages > 0 ? n - kStages : 0; k < n; ++k)
-        mbar_wait(full_bar(k % kStages), (uint32_t)(k / kStages) & 1u, &never, p.status);
-    }
-  } else {
-    // ---- consumers: threads 0-127 rowwise, 128-255 transposed ----
-    uint32_t off[8];
-    ColRole col{};
-    if (t < 128) row_offsets(t, off);
-    else col = col_role(t - 128, off);
-    int n = 0;
-    for (uint32_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x, ++n) {
-      const int s = n % kStages;
-      if (!mbar_wait(full_bar(s), (uint32_t)(n / kStages) & 1u, abort, p.status)) break;
-      const uint32_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
-      const int64_t m0 = (int64_t)tm * kRowsPerTile, c0 = (int64_t)tc * kColsPerTile;
-      const int valid = p.rows - m0 < kRowsPerTile ? (int)(p.rows - m0) : kRowsPerTile;  // 64 or 128
-      const uint32_t tile = ring + (uint32_t)s * kTileBytes;
-      if (t < 128) {
-        if (kRow && t < valid) encode_row(tile, off, m0 + t, c0, p.cols, p.orow);
-      } else if (kT) {
-        if (64 * (col.rb >> 1) < valid) encode_cols(tile, off, col, m0, c0, p.rows, p.ot);  // warp-uniform
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
-    }
-  }
-  __syncthreads();
-}
-
-// 2D map over x [rows, cols] BF16: box 64 columns x 128 rows, 128-byte
-// swizzle; rows past the end of x read as zeros.
-bool make_x_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols) {
-  auto fn = tensor_map_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {kColsPerTile, kRowsPerTile};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  });
 }
 
 template <bool kRow, bool kT>
@@ -317,11 +228,11 @@ cudaError_t launch(const CUtensorMap& map, const MxParams& p, unsigned grid, cud
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
     const cudaError_t e =
-        cudaFuncSetAttribute(mx_quant_kernel<kRow, kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(mx_quant_kernel<kRow, kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  mx_quant_kernel<kRow, kT><<<grid, kThreads, kSmemBytes, s>>>(map, p);
+  mx_quant_kernel<kRow, kT><<<grid, kRingThreads, kRingSmemBytes, s>>>(map, p);
   count_launch();
   return cudaGetLastError();
 }
@@ -336,13 +247,12 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows, int64_t cols, const nvf
   if (out_row) p.orow = MxOut{out_row->codes, out_row->scales, out_row->scale_layout};
   if (out_t) p.ot = MxOut{out_t->codes, out_t->scales, out_t->scale_layout};
   p.status = device_status_ptr();
-  const int64_t tiles = ((rows + kRowsPerTile - 1) / kRowsPerTile) * (cols / kColsPerTile);
-  if (tiles >= kMaxTiles) return cudaErrorInvalidValue;
+  const int64_t tiles = ring_tiles(rows, cols);
+  if (tiles >= kRingMaxTiles) return cudaErrorInvalidValue;
   if (tiles == 0) return cudaSuccess;
   CUtensorMap map;
-  if (!make_x_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
-  const int64_t cap = (int64_t)device_sm_count() * kCtasPerSm;
-  const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
+  if (!make_ring_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
+  const unsigned grid = ring_grid(tiles, kCtasPerSm);
   if (out_row && out_t) return launch<true, true>(map, p, grid, s);
   if (out_t) return launch<false, true>(map, p, grid, s);
   return launch<true, false>(map, p, grid, s);

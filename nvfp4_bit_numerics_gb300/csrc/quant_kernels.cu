@@ -1,23 +1,27 @@
 // quant_kernels.cu -- the NVFP4 quantization kernels for sm_103a: global
-// amax, 1x16 rowwise quantization, the 128x64 tile kernel that writes the
-// rowwise and/or the transposed (token-major, Hadamard-transformed) operand
-// from one read, and the 16x16 2D weight quantization that writes W and W^T.
+// amax, 1x16 rowwise quantization (round-to-nearest-even on the TMA tile ring
+// of tile_ring.cuh, stochastic rounding with per-thread loads), the 128x64
+// tile kernel that writes the rowwise and/or the transposed (token-major,
+// Hadamard-transformed) operand from one read, and the 16x16 2D weight
+// quantization that writes W and W^T.
 //
 // Method: "Pretraining Large Language Models with NVFP4" (gist.science
 // summary), Resumo técnico §2 Metodologia: two-level NVFP4 scaling ("Escala
 // em Dois Níveis"), random Hadamard transform on the Wgrad inputs (item 2),
 // 2D 16x16 weight scaling (item 3), stochastic rounding of gradients (item 4).
 //
-// All kernels read BF16 with 16-byte vector loads, keep their working set in
-// registers or a small shared-memory tile, and write packed codes with 8- or
-// 16-byte stores.  The plain amax and the RNE passes are bound by HBM
-// bandwidth; the passes that transform (Hadamard) or round stochastically
-// (Philox and the rounding itself per element) are bound by instruction
-// throughput, which is what their arithmetic is arranged to minimise.
+// The kernels read BF16 with 16-byte vector loads or TMA tiles, keep their
+// working set in registers or a small shared-memory tile, and write packed
+// codes with 8- or 16-byte stores.  The plain amax and the RNE passes are
+// bound by HBM bandwidth; the passes that transform (Hadamard) or round
+// stochastically (Philox and the rounding itself per element) are bound by
+// instruction throughput, which is what their arithmetic is arranged to
+// minimise.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "tile_ring.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -152,7 +156,8 @@ __device__ __forceinline__ float tensor_prologue(const float* amax, float* ts_ou
 }
 
 // ---------------------------------------------------------------------------
-// 1x16 rowwise quantization: one thread per 64 elements (4 blocks) of a row.
+// 1x16 rowwise quantization with stochastic rounding: one thread per 64
+// elements (4 independent blocks) of a row, read with 16-byte global loads.
 // ---------------------------------------------------------------------------
 template <bool kSR, bool kRHT>
 __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t* __restrict__ x, int64_t rows,
@@ -194,6 +199,54 @@ __global__ void __launch_bounds__(kThreads) quant_rowwise_kernel(const uint16_t*
     cp[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
     *reinterpret_cast<uint32_t*>(scales + sf_offset(layout, r, c0 >> 4, n_kb)) = sc;
   }
+}
+
+// ---------------------------------------------------------------------------
+// 1x16 rowwise round-to-nearest-even quantization on the TMA tile ring
+// (tile_ring.cuh): 128 x 64 tiles stream into a shared-memory ring while the
+// 8 consumer warps encode; thread t takes row t/2 of the tile, elements
+// 32 (t%2) .. +31 (2 blocks: 16 code bytes, two scale bytes), with the 16-point
+// transform along each 16-chunk when asked.  The row reads of 8 threads (4
+// rows x 2 halves) fall on 8 different swizzle chunks, free of bank
+// conflicts.  Used for the rowwise RNE kinds, which are bound by HBM; the
+// stochastic-rounding kinds, bound by instruction throughput, keep
+// quant_rowwise_kernel, whose threads hold 4 independent blocks each.
+// ---------------------------------------------------------------------------
+template <bool kRHT>
+__global__ void __launch_bounds__(kRingThreads, 3)
+    quant_rowwise_ring_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int64_t cols,
+                              const float* amax, uint8_t* codes, uint8_t* scales, int layout, float* ts_out,
+                              uint64_t seed, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float enc_tab[128];
+  const int t = threadIdx.x;
+  const float s_enc = tensor_prologue(amax, ts_out, status);
+  fill_enc_table(enc_tab, s_enc, t);
+  const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
+  const int r = t >> 1, hh = t & 1;
+  uint32_t roff[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) roff[i] = ring_chunk(r, 4 * hh + i);
+  const PhiloxKey no_key{};  // round-to-nearest-even draws no random numbers
+  tile_ring(&xmap, rows, cols, status, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
+    if (r >= valid) return;
+    const int64_t gr = m0 + r, gc = c0 + 32 * hh;
+    uint32_t cw[4], sc = 0;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float v[16];
+      unpack8(lds128(tile + roff[2 * b]), v);
+      unpack8(lds128(tile + roff[2 * b + 1]), v + 8);
+      if constexpr (kRHT) rht16(v, smask);
+      uint32_t E;
+      const uint2 o = quantize16<false>(v, s_enc, enc_tab, E, no_key, 0, 0);
+      cw[2 * b] = o.x;
+      cw[2 * b + 1] = o.y;
+      sc |= E << (8 * b);
+    }
+    *reinterpret_cast<uint4*>(codes + gr * (cols >> 1) + (gc >> 1)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    *reinterpret_cast<uint16_t*>(scales + sf_offset(layout, gr, gc >> 4, cols >> 4)) = (uint16_t)sc;
+  });
 }
 
 // ---------------------------------------------------------------------------
@@ -487,9 +540,38 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, float* plain,
   return cudaGetLastError();
 }
 
+namespace {
+
+template <bool kRHT>
+cudaError_t launch_rowwise_ring(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor& out,
+                                const float* amax, uint64_t seed, cudaStream_t s) {
+  const int64_t tiles = ring_tiles(rows, cols);
+  if (tiles >= kRingMaxTiles) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  if (!make_ring_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
+  auto kern = quant_rowwise_ring_kernel<kRHT>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  kern<<<ring_grid(tiles, 3), kRingThreads, kRingSmemBytes, s>>>(map, rows, cols, amax, out.codes, out.scales,
+                                                                  out.scale_layout, out.tensor_scale, seed,
+                                                                  device_status_ptr());
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_quant_rowwise(const void* x, int64_t rows, int64_t cols, const nvfp4_tensor& out,
                                  const float* amax, bool rht, bool sr, uint64_t seed, uint32_t stream_id,
                                  cudaStream_t s) {
+  if (!sr) return rht ? launch_rowwise_ring<true>(x, rows, cols, out, amax, seed, s)
+                      : launch_rowwise_ring<false>(x, rows, cols, out, amax, seed, s);
   const int64_t units = rows * (cols / 64);
   if (units >= kMaxUnits) return cudaErrorInvalidValue;
   const int grid = grid_for(units, 8);
@@ -498,13 +580,8 @@ cudaError_t launch_quant_rowwise(const void* x, int64_t rows, int64_t cols, cons
     kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), rows, cols, amax, out.codes, out.scales,
                                    out.scale_layout, out.tensor_scale, seed, key, stream_id, device_status_ptr());
   };
-  if (sr) {
-    if (rht) args(quant_rowwise_kernel<true, true>);
-    else args(quant_rowwise_kernel<true, false>);
-  } else {
-    if (rht) args(quant_rowwise_kernel<false, true>);
-    else args(quant_rowwise_kernel<false, false>);
-  }
+  if (rht) args(quant_rowwise_kernel<true, true>);
+  else args(quant_rowwise_kernel<true, false>);
   count_launch();
   return cudaGetLastError();
 }
