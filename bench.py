@@ -709,6 +709,8 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line, one line per further configured shape")
+    ap.add_argument("--quant-sweep", action="store_true",
+                    help="instead of the benchmark line, only the quantize-only sweep of --sweep")
     ap.add_argument("--next", action="store_true",
                     help="instead of the benchmark line, the further paths: GEMM-epilogue amax, the MXFP4 "
                          "layer step, a BF16 layer step")
@@ -722,6 +724,17 @@ def main():
         return run_sweep(args, rank, world, local)
     if args.next:
         return run_next(args, rank, world, local)
+    if args.quant_sweep:
+        if rank == 0:
+            import torch
+
+            from nvfp4_bit_numerics_gb300 import binding as B, build as nbuild
+
+            dev = torch.device("cuda", local)
+            nbuild.build()
+            B.load_library()
+            run_quant_sweep(torch.cuda.current_stream(dev), dev)
+        return 0
     return run_gpu(args, rank, world, local)
 
 
