@@ -108,3 +108,51 @@ def test_concurrent_host_threads():
     for i in range(2):
         for got, want in zip(results[i], refs[i]):
             assert torch.equal(got, want), i
+
+
+def test_graph_capture_of_the_further_paths():
+    """The MXFP4 quantize + GEMM, the GEMM with its output quantized in the
+    epilogue and the BF16 layer step, captured into one graph after a first
+    eager run (which creates the library's cuBLAS handle and sets kernel
+    attributes): every replay gives the eager results exactly."""
+    M, K, N = SHAPE
+    x, w, dy = inputs(21)
+    s = torch.cuda.Stream()
+    qx, qw = B.empty_mx_qtensor(M, K), B.empty_mx_qtensor(N, K)
+    nqx, nqw = B.empty_qtensor(M, K), B.empty_qtensor(N, K)
+    y_mx = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    y_bf = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    y_nv = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    yq = B.empty_qtensor(M, N)
+    amax = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def work():
+        B.nvfp4_quantize_mx(x, out=qx, stream=s)
+        B.nvfp4_quantize_mx(w, out=qw, stream=s)
+        B.nvfp4_gemm(qx, qw, out=y_mx, stream=s)
+        B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE, out=nqx, stream=s)
+        B.nvfp4_quantize(w, B.NVFP4_Q_2D, out=nqw, stream=s)
+        B.nvfp4_gemm_quant(nqx, nqw, yq, out=y_nv, amax_out=amax, stream=s)
+        B.nvfp4_linear_bf16_fwd(x, w, y=y_bf, stream=s)
+        B.nvfp4_linear_bf16_bwd(dy, x, w, dx=dx, dw=dw, stream=s)
+
+    outs = (y_mx, qx.codes, qx.scales, y_nv, yq.codes, yq.scales, amax, y_bf, dx, dw)
+    with torch.cuda.stream(s):
+        yq.amax.fill_(4.0)  # a given (delayed) amax for the quantized output
+        work()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        work()
+    for _ in range(2):
+        for t in outs:
+            t.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for got, want in zip(outs, ref):
+            assert torch.equal(got, want)
+    assert B.nvfp4_get_status() == B.NVFP4_OK
