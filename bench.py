@@ -127,18 +127,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def gemm_code_hash():
+    """sha256 of gemm_kernel.cu with its comments and blank lines removed:
+    the code the counters were taken on (comment edits keep it)."""
+    import re
+
+    src = os.path.join(ROOT, "nvfp4_bit_numerics_gb300", "csrc", "gemm_kernel.cu")
+    with open(src) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()
+
+
 def traffic_record():
     """DRAM bytes per GEMM launch from the committed ncu summary, valid only
-    while the GEMM source is unchanged since the capture."""
+    while the GEMM code is unchanged since the capture."""
     p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
-    src = os.path.join(ROOT, "nvfp4_bit_numerics_gb300", "csrc", "gemm_kernel.cu")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()
-    if rec.get("gemm_kernel_sha256") != h:
+    if rec.get("gemm_kernel_code_sha256") != gemm_code_hash():
         return None
     return rec.get("dram_bytes_per_launch")
 

@@ -511,6 +511,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //               stores.  (Per-lane 16-byte global stores -- 32 rows per warp
 //               instruction -- flooded the memory pipeline at every tile
 //               boundary and held up the barrier traffic of the main loop.)
+//               Optionally each lane also takes the max |D| of its values
+//               (amax_out) and quantizes its row's 128 BF16 values to NVFP4
+//               1x16 blocks with a given tensor amax (q_codes), writing the
+//               codes and MMA-layout scales itself.
 // ---------------------------------------------------------------------------
 constexpr int kPairBN = 256;
 constexpr int kPairABytes = 128 * kBKBytes;  // per CTA
