@@ -397,6 +397,18 @@ uint64_t nvfp4_kernel_launch_count(void);
  */
 void nvfp4_debug_stall_next_gemm(int32_t on);
 
+/*
+ * nvfp4_debug_stall_next_quantize -- the same test hook for the quantize
+ * kernels fed by a TMA tile pipeline (nvfp4_quantize_mx, and nvfp4_quantize
+ * of the rowwise round-to-nearest-even kinds).  With on != 0, the next such
+ * launch never loads the first tile of its first CTA; that CTA's wait for it
+ * runs into its bound (about 2 s), the kernel stops, waits (bounded) for the
+ * loads it did issue and returns; nvfp4_get_status then reports
+ * NVFP4_ERR_TIMEOUT and the CUDA context stays usable.  The output of that
+ * launch is unspecified.  The flag applies to one launch only.
+ */
+void nvfp4_debug_stall_next_quantize(int32_t on);
+
 #ifdef __cplusplus
 }
 #endif

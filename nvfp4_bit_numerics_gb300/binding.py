@@ -46,7 +46,7 @@ EXPORTED = [
     "nvfp4_linear_fwd", "nvfp4_linear_bwd", "nvfp4_linear_get_views", "nvfp4_get_status",
     "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
     "nvfp4_debug_stall_next_gemm", "nvfp4_gemm_amax", "nvfp4_quantize_mx", "nvfp4_mx_scale_bytes",
-    "nvfp4_linear_bf16_fwd", "nvfp4_linear_bf16_bwd", "nvfp4_gemm_quant",
+    "nvfp4_linear_bf16_fwd", "nvfp4_linear_bf16_bwd", "nvfp4_gemm_quant", "nvfp4_debug_stall_next_quantize",
 ]
 
 
@@ -101,6 +101,7 @@ def load_library(path=LIB_PATH):
         "nvfp4_kernel_launch_count": (U64, []),
         "nvfp4_linear_fwd_noalloc": (I32, [P, P, I64, I64, I64, U64, P, P]),
         "nvfp4_debug_stall_next_gemm": (None, [I32]),
+        "nvfp4_debug_stall_next_quantize": (None, [I32]),
         "nvfp4_quantize_mx": (I32, [P, I64, I64, I32, T, T, P]),
         "nvfp4_mx_scale_bytes": (SZ, [I64, I64, I32]),
         "nvfp4_linear_bf16_fwd": (I32, [P, P, I64, I64, I64, P, P]),
@@ -362,6 +363,10 @@ def nvfp4_get_status(stream=None):
 
 def nvfp4_debug_stall_next_gemm(on=True):
     load_library().nvfp4_debug_stall_next_gemm(1 if on else 0)
+
+
+def nvfp4_debug_stall_next_quantize(on=True):
+    load_library().nvfp4_debug_stall_next_quantize(1 if on else 0)
 
 
 def nvfp4_kernel_launch_count():

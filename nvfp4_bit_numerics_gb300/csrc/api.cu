@@ -71,6 +71,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn() {
   return fn;
 }
 
+std::atomic<int>& ring_debug_stall_flag() {
+  static std::atomic<int> flag{0};
+  return flag;
+}
+
 int device_sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -117,6 +122,8 @@ const char* nvfp4_status_string(nvfp4_status s) {
 uint64_t nvfp4_kernel_launch_count(void) { return g_launches.load(); }
 
 void nvfp4_debug_stall_next_gemm(int32_t on) { set_gemm_debug_stall(on); }
+
+void nvfp4_debug_stall_next_quantize(int32_t on) { ring_debug_stall_flag().store(on ? 1 : 0); }
 
 nvfp4_status nvfp4_get_status(nvfp4_stream stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;

@@ -61,6 +61,10 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows, int64_t cols, const nvf
 // stage's loads, so its bounded waits run out (gemm_kernel.cu).
 void set_gemm_debug_stall(int on);
 
+// The same for the next TMA-ring quantize launch (tile_ring.cuh): CTA 0 never
+// loads its first tile.  The flag lives in api.cu.
+std::atomic<int>& ring_debug_stall_flag();
+
 // GEMM launcher (gemm_kernel.cu).  Arguments are already validated.  With
 // amax_out set (a zeroed device float), the epilogue also takes the max |D|
 // over the BF16 (or FP32) output into it.  With yq set (BF16 output, M and N

@@ -46,6 +46,7 @@ struct MxParams {
   int64_t rows, cols;
   MxOut orow, ot;
   uint32_t* status;
+  int debug_stall;  // failure-detection test hook (tile_ring)
 };
 
 // UE8M0 code of a block whose max |x| has the BF16 bits `amax16` (sign clear,
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kRingThreads, kCtasPerSm) mx_quant_kernel(cons
   ColRole col{};
   if (t < 128) row_offsets(t, off);
   else if (t < 256) col = col_role(t - 128, off);
-  tile_ring(&xmap, p.rows, p.cols, p.status, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
+  tile_ring(&xmap, p.rows, p.cols, p.status, p.debug_stall, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
     if (t < 128) {
       if (kRow && t < valid) encode_row(tile, off, m0 + t, c0, p.cols, p.orow);
     } else if (kT) {
@@ -247,6 +248,7 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows, int64_t cols, const nvf
   if (out_row) p.orow = MxOut{out_row->codes, out_row->scales, out_row->scale_layout};
   if (out_t) p.ot = MxOut{out_t->codes, out_t->scales, out_t->scale_layout};
   p.status = device_status_ptr();
+  p.debug_stall = take_ring_debug_stall();
   const int64_t tiles = ring_tiles(rows, cols);
   if (tiles >= kRingMaxTiles) return cudaErrorInvalidValue;
   if (tiles == 0) return cudaSuccess;

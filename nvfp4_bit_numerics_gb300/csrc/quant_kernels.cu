@@ -216,7 +216,7 @@ template <bool kRHT>
 __global__ void __launch_bounds__(kRingThreads, 3)
     quant_rowwise_ring_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int64_t cols,
                               const float* amax, uint8_t* codes, uint8_t* scales, int layout, float* ts_out,
-                              uint64_t seed, uint32_t* status) {
+                              uint64_t seed, uint32_t* status, int debug_stall) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ float enc_tab[128];
   const int t = threadIdx.x;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kRingThreads, 3)
 #pragma unroll
   for (int i = 0; i < 4; ++i) roff[i] = ring_chunk(r, 4 * hh + i);
   const PhiloxKey no_key{};  // round-to-nearest-even draws no random numbers
-  tile_ring(&xmap, rows, cols, status, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
+  tile_ring(&xmap, rows, cols, status, debug_stall, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
     if (r >= valid) return;
     const int64_t gr = m0 + r, gc = c0 + 32 * hh;
     uint32_t cw[4], sc = 0;
@@ -560,7 +560,7 @@ cudaError_t launch_rowwise_ring(const void* x, int64_t rows, int64_t cols, const
   }
   kern<<<ring_grid(tiles, 3), kRingThreads, kRingSmemBytes, s>>>(map, rows, cols, amax, out.codes, out.scales,
                                                                   out.scale_layout, out.tensor_scale, seed,
-                                                                  device_status_ptr());
+                                                                  device_status_ptr(), take_ring_debug_stall());
   count_launch();
   return cudaGetLastError();
 }

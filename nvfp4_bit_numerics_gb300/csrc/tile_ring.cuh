@@ -59,9 +59,12 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 // the kernel's dynamic shared memory (kRingSmemBytes).  Everything the
 // consumers set up before the call is ordered before the first tile by the
 // barrier below.
+// With debug_stall set (a failure-detection test hook), CTA 0 never issues
+// the load of its first tile: its consumers' wait for that tile runs into its
+// bound, the kernel reports NVFP4_ERR_TIMEOUT and returns.
 template <class Consume>
 __device__ __forceinline__ void tile_ring(const CUtensorMap* xmap, int64_t rows, int64_t cols, uint32_t* status,
-                                          uint8_t* smem_raw, Consume&& consume) {
+                                          int debug_stall, uint8_t* smem_raw, Consume&& consume) {
   __shared__ __align__(8) uint64_t bars[2 * kRingStages];  // full[s], empty[s]
   __shared__ int abort_flag;
   const uint32_t raw = smem_u32(smem_raw);
@@ -90,6 +93,7 @@ __device__ __forceinline__ void tile_ring(const CUtensorMap* xmap, int64_t rows,
         const int s = n % kRingStages;
         if (n >= kRingStages && !mbar_wait(empty_bar(s), (uint32_t)((n / kRingStages) - 1) & 1u, abort, status))
           break;
+        if (debug_stall && n == 0 && blockIdx.x == 0) continue;  // nothing issued or armed for this tile
         const uint32_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
         mbar_arrive_expect_tx(full_bar(s), kRingTileBytes);
         tma_load_2d(ring + (uint32_t)s * kRingTileBytes, xmap, (int)(tc * kRingTileCols), (int)(tm * kRingTileRows),
@@ -117,6 +121,9 @@ __device__ __forceinline__ void tile_ring(const CUtensorMap* xmap, int64_t rows,
   }
   __syncthreads();
 }
+
+// The failure-detection test flag of the next ring launch (taken once).
+inline int take_ring_debug_stall() { return ring_debug_stall_flag().exchange(0); }
 
 // 2D map over x [rows, cols] BF16 with the ring's box (64 columns x 128
 // rows, 128-byte swizzle); rows past the end read as zeros.

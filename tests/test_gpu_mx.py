@@ -231,3 +231,39 @@ def test_mx_full_size_sampled():
     assert_mx_equal(qxt, mx.quantize_mx(np.ascontiguousarray(xf[:, ks].T)), rows=ks, what="full X^T")
     ys = y[torch.from_numpy(rs).cuda()][:, torch.from_numpy(cs).cuda()].float().cpu().numpy()
     assert rel_fro(ys, formats.float64_to_bf16_rne(mx.gemm_mx_ref(rx, rw))) <= 1e-3
+
+
+@pytest.mark.parametrize("which", ["mxfp4", "nvfp4_rowwise_rne"])
+def test_tile_ring_wait_bound_reports_timeout(which):
+    """Failure detection without a GPU fault for the TMA-ring quantizers: the
+    test hook makes the next launch skip its first CTA's first tile load, the
+    bounded wait runs out (about 2 s), the kernel drains what it issued and
+    reports NVFP4_ERR_TIMEOUT, and the next launch on the same context is
+    bit-exact again."""
+    import time
+
+    x = mx_edge_tensor(256, 512, 31)
+    xf = f32(x)
+    xg = x.cuda()
+
+    def run():
+        if which == "mxfp4":
+            return B.nvfp4_quantize_mx(xg, B.NVFP4_Q_ROWWISE)[0]
+        return B.nvfp4_quantize(xg, B.NVFP4_Q_ROWWISE, B.NVFP4_ROUND_RNE)[0]
+
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    B.nvfp4_debug_stall_next_quantize(True)
+    t0 = time.time()
+    run()
+    st = B.nvfp4_get_status()
+    dt = time.time() - t0
+    assert st == B.NVFP4_ERR_TIMEOUT
+    assert 1.0 < dt < 30.0
+    q = run()
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    if which == "mxfp4":
+        assert_mx_equal(q, mx.quantize_mx(xf), what="after the timeout")
+    else:
+        from tests.gpu_util import assert_q_equal
+
+        assert_q_equal(q, quant.quantize_1d(xf, "rne"), what="after the timeout")
