@@ -133,3 +133,40 @@ def test_linear_bf16_matches_loop_brute_force():
     for j in range(N):
         for k in range(K):
             assert Fraction(dw[j, k]) == sum(F(dy[i, j]) * F(x[i, k]) for i in range(M))
+
+
+def test_linear_layer_amax_is_the_quantized_tensors_own():
+    """The per-tensor scale of every operand is set from the amax of the
+    tensor actually quantized -- after the Hadamard transform for the two
+    Wgrad operands -- so the block holding that tensor's largest value gets
+    the largest E4M3 scale, 448 (code 0x7E), and ts = 1 / (2688 / amax).
+    The transformed amax is checked against an explicit float64 product of
+    Q = 1/4 H diag(s) on every 16-token chunk (not the oracle's tree)."""
+    x, w, dy = workloads.tiny_layer()
+    x, w, dy = (workloads.bf16_to_f32_numpy(t) for t in (x, w, dy))
+    seed = 77
+    f = linear.linear_fwd(x, w, seed)
+    b = linear.linear_bwd(dy, f, seed)
+    Q = rht.rht_matrix_f64(rht.rht_signs(seed))
+
+    def transformed_t(t):
+        # Q along the token axis (axis 0) in float64, returned transposed [cols, M]
+        tt = t.astype(np.float64).T
+        return (tt.reshape(tt.shape[0], -1, 16) @ Q.T).reshape(tt.shape)
+
+    def check(q, plain, blocks_2d=False):
+        amax = np.float32(np.max(np.abs(plain)))
+        assert abs(float(q["amax"]) - float(amax)) <= 4 * float(np.spacing(amax)), (q["amax"], amax)
+        assert q["ts"] == np.float32(np.float32(1) / np.float32(np.float32(2688) / q["amax"]))
+        r, c = np.unravel_index(np.argmax(np.abs(plain)), plain.shape)
+        E = q["scales_2d"][r // 16, c // 16] if blocks_2d else q["scales"][r, c // 16]
+        assert E == 0x7E, (r, c, E)
+
+    check(f["xq"], x)
+    check(f["wq"], w, blocks_2d=True)
+    check(f["xtq"], transformed_t(x))
+    check(b["dyq"], dy)
+    check(b["dytq"], transformed_t(dy))
+    # the transform moves the maximum: the untransformed amax is not the one used
+    assert b["dytq"]["amax"] != np.float32(np.max(np.abs(dy)))
+    assert f["xtq"]["amax"] != np.float32(np.max(np.abs(x)))

@@ -219,3 +219,60 @@ def test_swizzle_is_a_padded_bijection():
     E = np.zeros((256, 8), np.uint8)
     E[33, 5] = 7
     assert np.flatnonzero(quant.swizzle_scales(E)).tolist() == [533]
+
+
+def _ulp_close(a, b, ulps=4):
+    a, b = np.float32(a), np.float32(b)
+    return abs(float(a) - float(b)) <= ulps * float(np.spacing(max(abs(a), abs(b))))
+
+
+def test_amax_rht_closed_forms_pin_the_axis():
+    """Q = 1/4 H diag(s) maps a 16-chunk equal to c*s to (4c, 0, ..., 0)
+    (the first row of H is all ones, every other row sums to zero) and a
+    one-hot chunk v*e_k to values of magnitude |v|/4.  Both shapes are laid
+    along axis 0 (tokens) of a tensor whose two sizes differ, so the transform
+    along the wrong axis gives a different amax."""
+    seed = 31
+    s = rht.rht_signs(seed).astype(np.float32)
+    M, C = 48, 80
+    x = np.zeros((M, C), np.float32)
+    x[16:32, 5] = np.float32(3.0) * s          # chunk 1 of column 5: c = 3 -> 4c = 12
+    x[32 + 9, 70] = np.float32(-20.0)          # one-hot in chunk 2 of column 70: 20/4 = 5
+    assert quant.amax_rht(x, seed, axis=0) == np.float32(12.0)
+    assert quant.amax_rht(x, seed, axis=1) != np.float32(12.0)
+    # the one-hot alone: |v|/4 along either axis
+    y = np.zeros((M, C), np.float32)
+    y[32 + 9, 70] = np.float32(-20.0)
+    assert quant.amax_rht(y, seed, axis=0) == np.float32(5.0)
+    assert quant.amax_rht(y, seed, axis=1) == np.float32(5.0)
+    # a sign vector other than the layer's does not reach 4c
+    assert quant.amax_rht(x, seed + 1, axis=0) < np.float32(12.0)
+
+
+@pytest.mark.parametrize("axis", [0, 1])
+def test_amax_rht_slicing_and_independent_product(axis):
+    """The chunked loop (slices of whole 16-chunks along the other axis) gives
+    the same amax for every slice size, and it matches the transform written
+    as an explicit float64 matrix product on every 16-chunk, to a few float32
+    ulps (the oracle sums in float32)."""
+    x = _data((64, 96), 11)
+    seed = 5
+    ref = quant.amax_rht(x, seed, axis)
+    for chunk in (16, 100, 1000, 1 << 21):
+        assert quant.amax_rht(x, seed, axis, chunk_elems=chunk) == ref
+    Q = rht.rht_matrix_f64(rht.rht_signs(seed))
+    xm = np.moveaxis(x.astype(np.float64), axis, -1)
+    v = xm.reshape(xm.shape[:-1] + (xm.shape[-1] // 16, 16)) @ Q.T
+    assert _ulp_close(ref, np.max(np.abs(v)))
+    # the maximum sits somewhere else than the untransformed tensor's
+    assert ref != quant.tensor_amax(x)
+    # a closed-form chunk (c*s -> 4c) in the last line along the other axis,
+    # which the last slice of every slice size must reach
+    s = rht.rht_signs(seed).astype(np.float32)
+    z = x.copy()
+    if axis == 0:
+        z[16:32, -1] = np.float32(1000.0) * s
+    else:
+        z[-1, 32:48] = np.float32(1000.0) * s
+    for chunk in (16, 100, 1000, 1 << 21):
+        assert quant.amax_rht(z, seed, axis, chunk_elems=chunk) == np.float32(4000.0)
