@@ -19,8 +19,10 @@
 // product of two K-major NVFP4 operands with FP32 accumulation.
 //
 // Two kernels.  For M and N multiples of 256, nvfp4_gemm_pair_kernel (CTA
-// pairs, 256 x 256 tiles, tcgen05.mma.cta_group::2; described before it
-// below).  Otherwise the single-CTA kernel, whose design is:
+// pairs, 256 x 256 tiles, tcgen05.mma.cta_group::2, scale tiles loaded with
+// each operand stage and copied into tensor memory by tcgen05.cp from the
+// MMA warp; described before it below).  Otherwise the single-CTA kernel,
+// whose design is:
 // (one CTA per SM, persistent over 128 x BN output tiles)
 //   warp 0      TMA producer: 2D tiled loads of the packed codes (128-byte
 //               rows, 128B swizzle) and 1D bulk loads of the scale tiles,
@@ -484,56 +486,49 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 // all 256 x 256, each CTA's tensor memory receiving its own 128 rows.  Per SM
 // this halves the MMA instructions and cuts the operand bytes per flop by a
 // third relative to the single-CTA kernel.
-//   warp 0      producer (both CTAs): waits its own `empty` barrier, loads
-//               its A and B halves; the copies signal the even CTA's `full`
-//               barrier, which the even CTA's producer armed for both.
-//   warp 14     scale producer (both CTAs): fills a ring of 4 shared-memory
-//               scale slots ahead of the staging warps, so scale loads are
-//               off the stage-to-stage critical path.
-//   warp 1      even CTA: MMA issuer with one barrier wait per stage
-//               (`sf_ready`, which the even CTA's staging warps arrive on only
-//               after `full`); commits multicast to both CTAs.
-//   warps 2-5   scale staging (both CTAs): global stage g uses the tensor-
-//               memory scale region g % 5; once the MMAs of stage g - 5 (the
-//               region's previous user) committed, copy stage g's scale tiles
-//               (128 rows of A, all 256 rows of B) from their shared-memory
-//               slot into the region, free the slot, and arrive on the even
-//               CTA's `sf_ready` barrier of the region.  The three rings
-//               (6 operand stages, 4 scale slots, 5 scale regions) are
-//               decoupled so the operand ring is as deep as shared memory
-//               allows.  A scale load is issued once the staging of the
-//               stage 4 earlier has freed its slot, and lands about 1 us
-//               later (a fourth slot, over three, was up to 3 % faster).
-//   warps 6-13  epilogue (both CTAs) for the CTA's 128 rows; they release
+//   warp 0      producer (both CTAs): waits its own `empty` barrier, then
+//               loads the stage: its A and B halves (2D tiles, 128-byte
+//               swizzle) and the stage's scale tiles (this CTA's 128 A rows,
+//               all 256 B rows) as 2D tiles of 8-byte words; every copy
+//               signals the even CTA's `full` barrier, which the even CTA's
+//               producer armed for both CTAs' bytes.
+//   warp 1      even CTA: the MMA warp.  The whole warp runs the loop in step
+//               (so descriptors and addresses stay warp-uniform) and one
+//               elected lane issues, per stage: 12 tcgen05.cp.32x128b.warpx4
+//               copies of the scale tiles from shared memory into the stage's
+//               tensor-memory scale region (replicated into the four lane
+//               quadrants, the layout the MMA reads), the 4 MMAs
+//               (tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale), and a
+//               commit that frees the stage in both CTAs.  Copies and MMAs
+//               issued by one thread execute in order, so the copies of a
+//               stage land before its MMAs read them.
+//   warps 2-9   epilogue (both CTAs) for the CTA's 128 rows; they release
 //               the accumulator with a remote arrive on the even CTA, then
 //               write BF16 output as 32-row x 16-column boxes staged in a
 //               1 KB shared-memory buffer per warp and sent with bulk tensor
-//               stores.  (Per-lane 16-byte global stores -- 32 rows per warp
-//               instruction -- flooded the memory pipeline at every tile
-//               boundary and held up the barrier traffic of the main loop.)
-//               Optionally each lane also takes the max |D| of its values
-//               (amax_out) and quantizes its row's 128 BF16 values to NVFP4
-//               1x16 blocks with a given tensor amax (q_codes), writing the
-//               codes and MMA-layout scales itself.
+//               stores.  Optionally each lane also takes the max |D| of its
+//               values (amax_out) and quantizes its row's 128 BF16 values to
+//               NVFP4 1x16 blocks with a given tensor amax (q_codes), writing
+//               the codes and MMA-layout scales itself.
 // ---------------------------------------------------------------------------
 constexpr int kPairBN = 256;
 constexpr int kPairABytes = 128 * kBKBytes;  // per CTA
 constexpr int kPairBBytes = 128 * kBKBytes;  // per CTA (half of B)
 constexpr int kPairSfaBytes = 4 * 512;      // this CTA's 128 A rows, 4 MMAs
 constexpr int kPairSfbBytes = 2 * 4 * 512;  // all 256 B rows, 4 MMAs
-constexpr int kPairSfSlotBytes = kPairSfaBytes + kPairSfbBytes;
-constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
-constexpr int kPairSfCols = 16 + 4 * (kPairBN / 32);            // tensor-memory scale columns per stage
-constexpr int kPairSfRegions = (512 - kPairBN) / kPairSfCols;     // 5 tensor-memory scale regions
-constexpr int kPairStages = 6;                                    // shared-memory operand stages
-constexpr int kPairSfSlots = 4;                                   // shared-memory scale ring
-constexpr int kPairEpiBufBytes = 1024;                            // per epilogue warp: 32 rows x 16 BF16
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes + kPairSfaBytes + kPairSfbBytes;  // 38 KB
+constexpr int kPairSfCols = 16 + 4 * (kPairBN / 32);  // tensor-memory scale columns per stage
+constexpr int kPairStages = 5;                        // shared-memory stages = tensor-memory scale regions
+static_assert(kPairBN + kPairStages * kPairSfCols <= 512, "accumulator + scale regions exceed tensor memory");
+static_assert(kPairStageBytes % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled tiles");
+constexpr int kPairEpiWarps = 8;
+constexpr int kPairFirstEpiWarp = 2;
+constexpr int kPairEpiBufBytes = 1024;  // per epilogue warp: 32 rows x 16 BF16
 constexpr int kPairBarBytes = 512;
-constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kPairSfSlots * kPairSfSlotBytes +
-                               kEpiWarps * kPairEpiBufBytes + kPairBarBytes + 1024;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kPairEpiWarps * kPairEpiBufBytes + kPairBarBytes + 1024;
 static_assert(kPairSmemBytes <= 232448, "pair kernel shared memory exceeds the 227 KB opt-in limit");
-constexpr int kPairThreads = kNumThreads + 32;  // + the scale producer warp
-constexpr int kPairSfProducerWarp = kNumThreads / 32;
+constexpr int kPairThreads = 32 * (kPairFirstEpiWarp + kPairEpiWarps);
+constexpr uint64_t kDrainNs = 50000;  // after an abort: time for loads already issued to land
 
 __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -542,11 +537,10 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
 }
 
 // Arrive on the even CTA's copy of a barrier.  The arrivals that use it
-// follow a completed tensor-memory access (tcgen05.wait::st / wait::ld) and a
+// follow a completed tensor-memory access (tcgen05.wait::ld) and a
 // tcgen05.fence::before_thread_sync, which order that access before the
 // arrive; there is no ordinary memory to release, so the odd CTA uses the
-// relaxed cluster-scope arrive (a cluster-scope release costs ~0.7 us here)
-// and the even CTA its local arrive.
+// relaxed cluster-scope arrive and the even CTA its local arrive.
 __device__ __forceinline__ void mbar_arrive_leader(uint32_t local_addr, uint32_t rank) {
   if (rank == 0) {
     mbar_arrive(local_addr);
@@ -597,6 +591,21 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
       : "memory");
 }
 
+// Shared-memory descriptor of one 512-byte scale tile for tcgen05.cp: 32 rows
+// of 16 bytes, no swizzle, core matrices of 8 rows x 16 bytes 128 bytes apart
+// (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t desc_sf_tile(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(128 >> 4) << 32) |
+         ((uint64_t)1 << 46);
+}
+
+// Copy a 32-row x 16-byte tile from this CTA's shared memory into tensor-memory
+// lanes 0-31 at column `taddr`, replicated into all four lane quadrants, in both
+// CTAs of the pair (each CTA from its own shared memory).
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar) {
   const uint16_t mask = 3;
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
@@ -609,29 +618,35 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// One lane of a converged warp is elected to issue.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                            const __grid_constant__ CUtensorMap tmap_d, Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t sf_base = base + kPairStages * kPairStageBytes;
-  const uint8_t* sf_base_ptr = base_ptr + kPairStages * kPairStageBytes;
-  const uint32_t epi_base = sf_base + kPairSfSlots * kPairSfSlotBytes;
-  const uint32_t bar_base = epi_base + kEpiWarps * kPairEpiBufBytes;
+  const uint32_t epi_base = base + kPairStages * kPairStageBytes;
+  const uint32_t bar_base = epi_base + kPairEpiWarps * kPairEpiBufBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + (bar_base - base));
-  // barrier slots: full[S], empty[S], sf_ready[T], sf_full[R], sf_empty[R], tmem_full, tmem_empty, mma_done
+  // barrier slots: full[S], empty[S], tmem_full, tmem_empty, mma_done
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (kPairStages + s); };
-  auto sf_bar = [&](int t) { return bar_base + 8u * (2 * kPairStages + t); };
-  auto sf_full_bar = [&](int r) { return bar_base + 8u * (2 * kPairStages + kPairSfRegions + r); };
-  auto sf_empty_bar = [&](int r) { return bar_base + 8u * (2 * kPairStages + kPairSfRegions + kPairSfSlots + r); };
-  const uint32_t tmem_full = bar_base + 8u * (2 * kPairStages + kPairSfRegions + 2 * kPairSfSlots);
+  const uint32_t tmem_full = bar_base + 8u * (2 * kPairStages);
   const uint32_t tmem_empty = tmem_full + 8u;
   const uint32_t mma_done = tmem_full + 16u;
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + kPairSfRegions + 2 * kPairSfSlots + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 3);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   uint32_t rank;
@@ -648,18 +663,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int t = 0; t < kPairSfRegions; ++t) mbar_init(sf_bar(t), 2 * kSfWarps);
-    for (int r = 0; r < kPairSfSlots; ++r) {
-      mbar_init(sf_full_bar(r), 1);
-      mbar_init(sf_empty_bar(r), kSfWarps);
-    }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 2 * kEpiWarps);
+    mbar_init(tmem_empty, 2 * kPairEpiWarps);
     mbar_init(mma_done, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_sfa)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_sfb)) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -685,155 +697,116 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
           if (p.debug_stall && tile == pair && ks == 0) {
-            // nothing is issued or armed for this stage: the consumers' bounded
-            // waits run out and the kernel reports NVFP4_ERR_TIMEOUT
+            // nothing is issued or armed for this stage: the MMA warp's
+            // bounded wait runs out and the kernel reports NVFP4_ERR_TIMEOUT
             if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
             continue;
           }
           const uint32_t sa = base + stage * kPairStageBytes;
           const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * (kPairABytes + kPairBBytes));
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * kPairStageBytes);
           tma_load_2d_pair(sa, &tmap_a, ks * kBKBytes, mb * 256 + (int)rank * 128, leader_full);
           tma_load_2d_pair(sa + kPairABytes, &tmap_b, ks * kBKBytes, nb * kPairBN + (int)rank * 128, leader_full);
+          // scale tiles as 8-byte words: 4 tiles (2 KB) of this CTA's A rows,
+          // 4 tiles of each of the two 128-row halves of B
+          tma_load_2d_pair(sa + kPairABytes + kPairBBytes, &tmap_sfa, ks * 256, 2 * mb + (int)rank, leader_full);
+          tma_load_2d_pair(sa + kPairABytes + kPairBBytes + kPairSfaBytes, &tmap_sfb, ks * 256, 2 * nb,
+                           leader_full);
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
-    }
-  } else if (warp == kPairSfProducerWarp) {
-    // ------------------------------ scale producer ------------------------
-    if (lane == 0) {
-      int slot = 0;
-      uint32_t sphase = 0;
-      for (int tile = pair; tile < n_tiles; tile += num_pairs) {
-        int mb, nb;
-        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
-        bool ok = true;
-        for (int ks = 0; ks < k_stages; ++ks) {
-          if (!mbar_wait(sf_empty_bar(slot), sphase ^ 1u, abort, p.status)) { ok = false; break; }
-          const int nk = (ks == k_stages - 1) ? last_nk : 4;
-          const uint32_t sf_bytes = (uint32_t)nk * 512u;
-          const uint32_t dst = sf_base + slot * kPairSfSlotBytes;
-          mbar_arrive_expect_tx(sf_full_bar(slot), 3u * sf_bytes);
-          bulk_load(dst, p.sfa + ((int64_t)(2 * mb + (int)rank) * p.sf_tiles_k + ks * 4) * 512, sf_bytes,
-                    sf_full_bar(slot));
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            bulk_load(dst + kPairSfaBytes + h * 2048, p.sfb + ((int64_t)(2 * nb + h) * p.sf_tiles_k + ks * 4) * 512,
-                      sf_bytes, sf_full_bar(slot));
-          if (++slot == kPairSfSlots) { slot = 0; sphase ^= 1u; }
+      // after an abort, loads already issued may still be in flight: give
+      // them time to land before the CTA can exit
+      if (*abort) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < kDrainNs) {
         }
-        if (!ok) break;
       }
     }
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer (even CTA) ------------------
-    // one instantiation per operand format, as in the single-CTA kernel
+    // ------------------------------ MMA warp (even CTA) --------------------
+    // lane 0 waits, the warp follows its verdict (uniform by construction)
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) {
+      int r = 0;
+      if (lane == 0) r = mbar_wait(bar, parity, abort, p.status) ? 1 : 0;
+      return __shfl_sync(0xFFFFFFFFu, r, 0) != 0;
+    };
+    // one instantiation per operand format: the issue path carries no
+    // format test
     auto issue = [&](auto mx_tag) {
       constexpr bool kMX = decltype(mx_tag)::value;
       const uint32_t idesc = idesc_block_scaled(256, kPairBN, kMX);
-      int stage = 0, region = 0;
-      uint32_t phase = 0, rphase = 0, acc_phase = 0;
+      const uint32_t tmem_u = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+      // descriptors of stage 0; stage s adds s * kPairStageBytes
+      const uint64_t da0 = desc_sw128(base), db0 = desc_sw128(base + kPairABytes);
+      const uint64_t dsf0 = desc_sf_tile(base + kPairABytes + kPairBBytes);
+      constexpr uint64_t kStageDesc = kPairStageBytes >> 4;
+      constexpr uint64_t kTileDesc = 512 >> 4;
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = pair; tile < n_tiles && ok; tile += num_pairs) {
-        if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort, p.status)) break;
+        if (!warp_wait(tmem_empty, acc_phase ^ 1u)) break;
         tc_fence_after();
         for (int ks = 0; ks < k_stages; ++ks) {
-          // sf_ready also covers `full`: the even CTA's staging warps wait for it
-          if (!mbar_wait(sf_bar(region), rphase, abort, p.status)) { ok = false; break; }
+          if (!warp_wait(full_bar(stage), phase)) { ok = false; break; }
           tc_fence_after();
-          const int nk = (ks == k_stages - 1) ? last_nk : 4;
-          const uint32_t sa = base + stage * kPairStageBytes;
-          uint64_t da = desc_sw128(sa), db = desc_sw128(sa + kPairABytes);
-          uint32_t sfa = tmem + (uint32_t)(kPairBN + region * kPairSfCols), sfb = sfa + 16;
-          for (int j = 0; j < nk; ++j) {
-            tc_mma_pair(tmem, da, db, idesc, sfa, sfb, (ks | j) != 0, kMX);
-            da += 2;  // +32 bytes along K inside the 128-byte swizzle atom
-            db += 2;
-            sfa += 4;
-            sfb += kPairBN / 32;
+          const uint64_t soff = (uint64_t)stage * kStageDesc;
+          const uint64_t da = da0 + soff, db = db0 + soff, dsf = dsf0 + soff;
+          const uint32_t sfa = tmem_u + (uint32_t)(kPairBN + stage * kPairSfCols), sfb = sfa + 16;
+          if (elect_one()) {
+            // scale tiles: A tile j -> columns 4j; B tile (j, h) -> 16 + 8j + 4h
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tc_cp_sf_pair(sfa + 4 * j, dsf + j * kTileDesc);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tc_cp_sf_pair(sfb + 8 * j + 4 * h, dsf + (4 + 4 * h + j) * kTileDesc);
+            if (ks != k_stages - 1 || last_nk == 4) {
+              tc_mma_pair(tmem_u, da, db, idesc, sfa, sfb, ks != 0, kMX);
+              tc_mma_pair(tmem_u, da + 2, db + 2, idesc, sfa + 4, sfb + 8, 1u, kMX);
+              tc_mma_pair(tmem_u, da + 4, db + 4, idesc, sfa + 8, sfb + 16, 1u, kMX);
+              tc_mma_pair(tmem_u, da + 6, db + 6, idesc, sfa + 12, sfb + 24, 1u, kMX);
+            } else {
+              // +32 bytes along K per MMA inside the 128-byte swizzle atom
+              for (int j = 0; j < last_nk; ++j)
+                tc_mma_pair(tmem_u, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + 8 * j, (ks | j) != 0, kMX);
+            }
+            tc_commit_pair_multicast(empty_bar(stage));
           }
-          tc_commit_pair_multicast(empty_bar(stage));
+          __syncwarp();
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
-          if (++region == kPairSfRegions) { region = 0; rphase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit_pair_multicast(tmem_full);
+        if (elect_one()) tc_commit_pair_multicast(tmem_full);
+        __syncwarp();
         acc_phase ^= 1u;
       }
     };
-    if (rank == 0 && lane == 0) {
+    if (rank == 0) {
       if (p.mx) issue(std::true_type{});
       else issue(std::false_type{});
-      tc_commit_pair(mma_done);
-      volatile int never = 0;
-      mbar_wait(mma_done, 0, &never, p.status);
-    }
-  } else if (warp < kFirstEpiWarp) {
-    // ---------------- scale factors: shared memory -> tensor memory -------------
-    // Same replicated layout as the single-CTA kernel: lane i, column c of a
-    // scale tile holds the c-th word of the 512-byte tile's 16-byte row i.
-    // A stage's columns are rewritten only after that stage's previous MMAs
-    // committed (`empty`); the shared-memory slot is freed after the copy.
-    const int q = warp & 3;
-    int g = 0, stage = 0, slot = 0, region = 0;
-    uint32_t phase = 0, sphase = 0, rphase = 0;
-    for (int tile = pair; tile < n_tiles; tile += num_pairs) {
-      bool ok = true;
-      for (int ks = 0; ks < k_stages; ++ks, ++g) {
-        int ready = 0;
-        if (lane == 0) {
-          // the region's previous user is stage g - 5: operand stage
-          // (g - 5) % 6, committed in round (g - 5) / 6
-          const int gp = g - kPairSfRegions;
-          ready = (mbar_wait(sf_full_bar(slot), sphase, abort, p.status) &&
-                   (gp < 0 || mbar_wait(empty_bar(gp % kPairStages), (uint32_t)(gp / kPairStages) & 1u, abort,
-                                        p.status)) &&
-                   (rank != 0 || mbar_wait(full_bar(stage), phase, abort, p.status))) ? 1 : 0;
-        }
-        ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
-        if (!ready) { ok = false; break; }
-        tc_fence_after();
-        const uint8_t* sfa_s = sf_base_ptr + slot * kPairSfSlotBytes;
-        const uint8_t* sfb_s = sfa_s + kPairSfaBytes;
-        uint32_t r[kPairSfCols];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 wa = *reinterpret_cast<const uint4*>(sfa_s + 512 * j + 16 * lane);
-          const uint4 w0 = *reinterpret_cast<const uint4*>(sfb_s + 512 * j + 16 * lane);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(sfb_s + 2048 + 512 * j + 16 * lane);
-          r[4 * j] = wa.x; r[4 * j + 1] = wa.y; r[4 * j + 2] = wa.z; r[4 * j + 3] = wa.w;
-          const int o = 16 + 8 * j;
-          r[o] = w0.x; r[o + 1] = w0.y; r[o + 2] = w0.z; r[o + 3] = w0.w;
-          r[o + 4] = w1.x; r[o + 5] = w1.y; r[o + 6] = w1.z; r[o + 7] = w1.w;
-        }
-        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kPairBN + region * kPairSfCols);
-#pragma unroll
-        for (int c = 0; c < kPairSfCols / 16; ++c) tmem_st16(taddr + 16 * c, r + 16 * c);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(sf_empty_bar(slot));
-          mbar_arrive_leader(sf_bar(region), rank);
-        }
-        if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
-        if (++slot == kPairSfSlots) { slot = 0; sphase ^= 1u; }
-        if (++region == kPairSfRegions) { region = 0; rphase ^= 1u; }
+      // every copy and MMA issued by this warp has finished
+      if (elect_one()) tc_commit_pair(mma_done);
+      __syncwarp();
+      if (lane == 0) {
+        volatile int never = 0;
+        mbar_wait(mma_done, 0, &never, p.status);
       }
-      if (!ok) break;
+      __syncwarp();
     }
   } else {
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;
-    const int half = (warp - kFirstEpiWarp) >> 2;
+    const int half = (warp - kPairFirstEpiWarp) >> 2;
     constexpr int kCols = kPairBN / 2;
     const float alpha = p.mx ? 1.0f : __fmul_rn(*p.ts_a, *p.ts_b);
     float q_senc = 1.0f;  // quantized output: the encode scale of its tensor amax
     if (p.q_codes) {
       const float a = *p.q_amax;
       q_senc = tensor_encode_scale(a);
-      if (blockIdx.x == 0 && warp == kFirstEpiWarp && lane == 0) {
+      if (blockIdx.x == 0 && warp == kPairFirstEpiWarp && lane == 0) {
         *p.q_ts = tensor_decode_scale(q_senc);
         if (!(abs_bits(a) < 0x7F800000u)) raise_status(p.status, kStatusNonFinite);
       }
@@ -884,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         // 32-byte swizzle (16-byte half h of row r at h ^ bit 2 of r), one
         // bulk tensor store per chunk; the buffer is rewritten once the
         // previous store has read it.
-        const uint32_t buf = epi_base + (uint32_t)(warp - kFirstEpiWarp) * kPairEpiBufBytes;
+        const uint32_t buf = epi_base + (uint32_t)(warp - kPairFirstEpiWarp) * kPairEpiBufBytes;
         const uint32_t sw = (uint32_t)((lane >> 2) & 1);
 #pragma unroll
         for (int j = 0; j < kCols / 16; ++j) {
@@ -982,6 +955,21 @@ bool make_out_map(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D map over an MMA-layout scale tensor as 8-byte words: one row per 128
+// tensor rows (tiles_k 512-byte tiles = tiles_k * 64 words), box = 4 tiles
+// (256 words, 2 KB) x box_rows rows.
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t tiles_k, uint64_t row_tiles, uint32_t box_rows) {
+  auto fn = tensor_map_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {tiles_k * 64, row_tiles};
+  cuuint64_t strides[1] = {tiles_k * 512};
+  cuuint32_t box[2] = {256, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() { return device_sm_count(); }
 
 template <int BN>
@@ -1043,10 +1031,12 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
       return NVFP4_ERR_CUDA;
     attr_set[dev] = true;
   }
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, msfa, msfb;
   const int64_t K = a.cols;
   if (!make_code_map(&ma, a.codes, (uint64_t)K / 2, (uint64_t)a.rows, 128) ||
-      !make_code_map(&mb, b.codes, (uint64_t)K / 2, (uint64_t)b.rows, 128))
+      !make_code_map(&mb, b.codes, (uint64_t)K / 2, (uint64_t)b.rows, 128) ||
+      !make_sf_map(&msfa, a.scales, (uint64_t)K / 64, (uint64_t)a.rows / 128, 1) ||
+      !make_sf_map(&msfb, b.scales, (uint64_t)K / 64, (uint64_t)b.rows / 128, 2))
     return NVFP4_ERR_CUDA;
   Params p;
   p.sfa = a.scales;
@@ -1078,7 +1068,7 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   const int tiles = (p.M / 256) * (p.N / kPairBN);
   const int pairs_max = sm_count() / 2;
   const int pairs = tiles < pairs_max ? tiles : pairs_max;
-  nvfp4_gemm_pair_kernel<<<2 * pairs, kPairThreads, kPairSmemBytes, s>>>(ma, mb, md, p);
+  nvfp4_gemm_pair_kernel<<<2 * pairs, kPairThreads, kPairSmemBytes, s>>>(ma, mb, msfa, msfb, md, p);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
