@@ -197,7 +197,8 @@ def test_pipeline_wait_bound_reports_timeout(M, N, K):
 
 
 @pytest.mark.parametrize("K,N,w2d,rht", [(4096, 4096, True, False), (5120, 5120, False, True),
-                                         (20480, 5120, True, False)])
+                                         (8192, 8192, False, False), (8192, 8192, False, True),
+                                         (5120, 20480, True, False), (20480, 5120, True, False)])
 def test_gemm_sweep_full_size_sampled(K, N, w2d, rht):
     """The GEMM shape sweep at full size (M = 16384, heavy-tailed X ~ t(3),
     W ~ N(0, 0.02)): X quantized 1x16, W with 16x16 blocks or 1x16, with or
