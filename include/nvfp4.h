@@ -282,7 +282,17 @@ nvfp4_status nvfp4_gemm_quant(const nvfp4_tensor* a, const nvfp4_tensor* b, cons
                               void* d_dev, int64_t ldd, float* amax_dev, nvfp4_stream stream);
 
 /*
- * One NVFP4 linear layer Y = X W^T, X [M, K] tokens x in-features, W [N, K].
+ * One NVFP4 linear layer Y = X W^T, X [M, K] tokens x in-features, W [N, K]:
+ * the three GEMMs of a training step -- Fprop, Dgrad and Wgrad -- with the
+ * quantization recipe of "Pretraining Large Language Models with NVFP4"
+ * (gist.science summary), Resumo técnico §2, "Técnicas de Treinamento
+ * Integradas": item 2 (random Hadamard transform on both Wgrad inputs, along
+ * the token dimension the Wgrad GEMM reduces over), item 3 (16x16 weight
+ * blocks, so the W of Fprop and the W^T of Dgrad are one quantization) and
+ * item 4 (stochastic rounding of the gradient dY, round-to-nearest-even for X
+ * and W), on the two-level NVFP4 format of the same section ("Formato NVFP4",
+ * "Escala em Dois Níveis": each operand's FP32 scale comes from the amax of
+ * the tensor actually quantized, after the transform where one applies).
  *
  * nvfp4_linear_fwd: amax of X, of the Hadamard-transformed X^T and of W;
  *   X -> rowwise RNE (Fprop operand) and X^T -> Hadamard + RNE (saved Wgrad
@@ -345,7 +355,11 @@ nvfp4_status nvfp4_linear_get_views(void* ws_dev, int64_t M, int64_t K, int64_t 
  * NVFP4_ERR_WORKSPACE before anything is launched.  Other size rules as
  * nvfp4_linear_fwd.
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
+ * device current) and keeps it for the rest of the process; make that first
+ * call before any stream capture.  A cudaDeviceReset (or any other reset of
+ * the device's primary context) reloads the library's device code at a new
+ * address, so this entry point must not be called on that device after such
+ * a reset in the same process.  Every
  * call shares the one array and leaves its contents behind; nothing in it has
  * to start at zero.  Calls whose work overlaps on the GPU (other streams, or
  * other host threads) race on the array: serialise them.  The quantized

@@ -248,13 +248,14 @@ cudaError_t launch_quant_mx(const void* x, int64_t rows, int64_t cols, const nvf
   if (out_row) p.orow = MxOut{out_row->codes, out_row->scales, out_row->scale_layout};
   if (out_t) p.ot = MxOut{out_t->codes, out_t->scales, out_t->scale_layout};
   p.status = device_status_ptr();
-  p.debug_stall = take_ring_debug_stall();
   const int64_t tiles = ring_tiles(rows, cols);
   if (tiles >= kRingMaxTiles) return cudaErrorInvalidValue;
   if (tiles == 0) return cudaSuccess;
   CUtensorMap map;
   if (!make_ring_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
   const unsigned grid = ring_grid(tiles, kCtasPerSm);
+  // the one-shot test flag is taken only by a call that launches
+  p.debug_stall = take_ring_debug_stall();
   if (out_row && out_t) return launch<true, true>(map, p, grid, s);
   if (out_t) return launch<false, true>(map, p, grid, s);
   return launch<true, false>(map, p, grid, s);

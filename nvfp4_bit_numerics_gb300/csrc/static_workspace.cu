@@ -24,8 +24,11 @@ constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;  // 32 MiB; stated in
 
 static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
 
-// Device address of g_static_workspace per device.  In host code the array's
-// name is only a host-side stand-in, never a device address.
+// Device address of g_static_workspace per device, looked up once with that
+// device current.  In host code the array's name is only a host-side
+// stand-in, never a device address.  A reset of the device's primary context
+// would move the array; calls after one are not supported (stated in
+// include/nvfp4.h).
 void* g_workspace_addr[64] = {nullptr};
 std::mutex g_workspace_mutex;
 

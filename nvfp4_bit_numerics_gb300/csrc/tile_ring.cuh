@@ -89,22 +89,29 @@ __device__ __forceinline__ void tile_ring(const CUtensorMap* xmap, int64_t rows,
   if (warp == kRingConsumerWarps) {
     if (lane == 0) {
       int n = 0;
+      uint32_t issued = 0;  // bit s: the latest tile of slot s had its load issued
       for (uint32_t tl = blockIdx.x; tl < n_tiles; tl += gridDim.x, ++n) {
         const int s = n % kRingStages;
         if (n >= kRingStages && !mbar_wait(empty_bar(s), (uint32_t)((n / kRingStages) - 1) & 1u, abort, status))
           break;
-        if (debug_stall && n == 0 && blockIdx.x == 0) continue;  // nothing issued or armed for this tile
+        if (debug_stall && n == 0 && blockIdx.x == 0) {  // nothing issued or armed for this tile
+          issued &= ~(1u << s);
+          continue;
+        }
         const uint32_t tm = tl / tiles_c, tc = tl - tm * tiles_c;
         mbar_arrive_expect_tx(full_bar(s), kRingTileBytes);
         tma_load_2d(ring + (uint32_t)s * kRingTileBytes, xmap, (int)(tc * kRingTileCols), (int)(tm * kRingTileRows),
                     full_bar(s));
+        issued |= 1u << s;
       }
       // every load this CTA issued has landed before it exits: the last
-      // kRingStages loads' phases (the earlier ones were consumed), each
-      // wait bounded and independent of the abort flag
+      // kRingStages tiles' phases (the earlier ones were consumed), skipping a
+      // tile whose load was never issued, each wait bounded and independent of
+      // the abort flag
       volatile int never = 0;
       for (int k = n - kRingStages > 0 ? n - kRingStages : 0; k < n; ++k)
-        mbar_wait(full_bar(k % kRingStages), (uint32_t)(k / kRingStages) & 1u, &never, status);
+        if ((issued >> (k % kRingStages)) & 1u)
+          mbar_wait(full_bar(k % kRingStages), (uint32_t)(k / kRingStages) & 1u, &never, status);
     }
   } else {
     int n = 0;
