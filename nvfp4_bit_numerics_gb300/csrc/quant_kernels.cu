@@ -250,14 +250,103 @@ __global__ void __launch_bounds__(kRingThreads, 3)
 }
 
 // ---------------------------------------------------------------------------
+// Packed float pairs: two IEEE float32 values in one 64-bit register pair,
+// operated on by the paired instructions (add/sub/mul/fma .rn.f32x2), which
+// round each half exactly as the scalar instruction would.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t p) { return __uint_as_float((uint32_t)p); }
+__device__ __forceinline__ float f2_hi(uint64_t p) { return __uint_as_float((uint32_t)(p >> 32)); }
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// a * b + c in one rounding per half
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// The two BF16 values of a 32-bit word as a float pair (element 0 low).
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) { return f2_pack(w << 16, w & 0xFFFF0000u); }
+
+// The 16-point transform Q = 1/4 H16 diag(s) on 16 pairs at once (two
+// independent vectors, one per half): the butterfly with strides 1, 2, 4, 8,
+// then * 0.25 + 0 in one rounding (as rht16_unsigned; the signs are applied
+// to the BF16 words before).
+__device__ __forceinline__ void rht16_pairs(uint64_t* p) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const uint64_t a = p[i], b = p[i + h];
+        p[i] = f2_add(a, b);
+        p[i + h] = f2_sub(a, b);
+      }
+    }
+  }
+  const uint64_t quarter = f2_pack(0x3E800000u, 0x3E800000u), zero = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = f2_fma(p[i], quarter, zero);
+}
+
+// One 1x16 block held as 8 pairs (elements 2j, 2j+1 in pair j): amax, scale,
+// 16 codes (8 bytes).  Same arithmetic as quantize16.
+template <bool kSR>
+__device__ __forceinline__ uint2 quantize16_pairs(const uint64_t* p, float s_enc, const float* enc_tab, uint32_t& E,
+                                                  const PhiloxKey& key, uint32_t stream, uint64_t e0) {
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(f2_lo(p[j])), fabsf(f2_hi(p[j]))));
+  float enc;
+  block_scale_tab(m, s_enc, enc_tab, E, enc);
+  const uint64_t enc2 = f2_pack(__float_as_uint(enc), __float_as_uint(enc));
+  float s[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint64_t q = f2_mul(p[j], enc2);
+    s[2 * j] = f2_lo(q);
+    s[2 * j + 1] = f2_hi(q);
+  }
+  if constexpr (kSR) {
+    uint32_t nu[16];
+    sr_nu16(key, stream, e0, nu);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = e2m1_sr_value(s[i], nu[i]);
+  }
+  uint2 out;
+  out.x = e2m1x8_rn(s);
+  out.y = e2m1x8_rn(s + 8);
+  return out;
+}
+
+// ---------------------------------------------------------------------------
 // Tile kernel: one read of x [rows, cols] BF16 per 128x64 tile, staged in
 // shared memory, then
 //  - rowwise:    1x16 blocks along cols of x       -> out_row [rows, cols]
 //  - transposed: 1x16 blocks along rows of x (after the optional 16-point
 //                transform along rows)             -> out_t   [cols, rows]
-// Persistent over tiles.  Thread t: rowwise, row t/2 and two 16-element
+// Persistent over tiles; the next tile's global loads are issued before the
+// current tile is encoded.  Thread t: rowwise, row t/2 and two 16-element
 // blocks; transposed, the column pair 2(t%32), 2(t%32)+1 over the 16 rows
-// 16(t/32)..16(t/32)+15 (one 32-bit shared-memory word per row).
+// 16(t/32)..16(t/32)+15 (one 32-bit shared-memory word per row), the two
+// columns carried as float pairs through the transform and the scaling.
 // ---------------------------------------------------------------------------
 struct TileOut {
   uint8_t* codes;
@@ -273,7 +362,7 @@ constexpr int kTileRows = 128;  // rows (tokens) per tile of the tile kernel
 constexpr int kTilePitch = 72;  // uint16 per smem row: 144 B, conflict-free 16 B row reads
 
 template <bool kRow, bool kT, bool kRHT, bool kSR>
-__global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(kThreads, 3) quant_tile_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                               int64_t cols, TileOut orow, TileOut ot,
                                                               uint64_t seed, const __grid_constant__ PhiloxKey key,
                                                               uint32_t* status) {
@@ -293,16 +382,22 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
   const uint32_t smask = kRHT ? rht_sign_mask(seed) : 0u;
 
   const uint32_t tiles_c32 = (uint32_t)tiles_c;  // tile counts < 2^32 (launcher): 32-bit index math
-  for (uint32_t tl = blockIdx.x; tl < (uint32_t)n_tiles; tl += gridDim.x) {
+  uint4 q[4];
+  auto load_tile = [&](uint32_t tl) {
     const uint32_t tm = tl / tiles_c32, tc = tl - tm * tiles_c32;
     const int64_t m0 = (int64_t)tm * kTileRows, c0 = (int64_t)tc * kTile;
-    const int valid = rows - m0 < kTileRows ? (int)(rows - m0) : kTileRows;  // 64 or 128
-    uint4 q[4];
+    const int valid = rows - m0 < kTileRows ? (int)(rows - m0) : kTileRows;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int v = t + k * kThreads;
       q[k] = (v >> 3) < valid ? ldg_nc_v4(x + (m0 + (v >> 3)) * cols + c0 + (v & 7) * 8) : make_uint4(0, 0, 0, 0);
     }
+  };
+  if (blockIdx.x < (uint32_t)n_tiles) load_tile(blockIdx.x);
+  for (uint32_t tl = blockIdx.x; tl < (uint32_t)n_tiles; tl += gridDim.x) {
+    const uint32_t tm = tl / tiles_c32, tc = tl - tm * tiles_c32;
+    const int64_t m0 = (int64_t)tm * kTileRows, c0 = (int64_t)tc * kTile;
+    const int valid = rows - m0 < kTileRows ? (int)(rows - m0) : kTileRows;  // 64 or 128
     __syncthreads();  // the previous tile's readers are done
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -310,6 +405,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
       *reinterpret_cast<uint4*>(&tile[(v >> 3) * kTilePitch + (v & 7) * 8]) = q[k];
     }
     __syncthreads();
+    if (tl + gridDim.x < (uint32_t)n_tiles) load_tile(tl + gridDim.x);
 
     if (kRow && (t >> 1) < valid) {
       const int r = t >> 1, hb = (t & 1) * 2;  // row, first of two blocks
@@ -318,12 +414,13 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const uint4* sp = reinterpret_cast<const uint4*>(&tile[r * kTilePitch + (hb + b) * 16]);
-        float v[16];
-        unpack8(sp[0], v);
-        unpack8(sp[1], v + 8);
+        const uint4 w0 = sp[0], w1 = sp[1];
+        const uint64_t pr[8] = {f2_from_bf16x2(w0.x), f2_from_bf16x2(w0.y), f2_from_bf16x2(w0.z),
+                                f2_from_bf16x2(w0.w), f2_from_bf16x2(w1.x), f2_from_bf16x2(w1.y),
+                                f2_from_bf16x2(w1.z), f2_from_bf16x2(w1.w)};
         uint32_t E;
         const uint2 o =
-            quantize16<kSR>(v, s_row, enc_tab[0], E, key, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
+            quantize16_pairs<kSR>(pr, s_row, enc_tab[0], E, key, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
         cw[2 * b] = o.x;
         cw[2 * b + 1] = o.y;
         sc |= E << (8 * b);
@@ -333,26 +430,47 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const uint16_t* __
     }
     if (kT && 16 * (t >> 5) < valid) {
       const int pc = (t & 31) * 2, ch = t >> 5;
-      float va[16], vb[16];
+      uint64_t p[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[(16 * ch + i) * kTilePitch + pc]);
         if constexpr (kRHT) w ^= rht_sign_word(smask, i);  // both columns are in row i
-        va[i] = bf16lo(w);
-        vb[i] = bf16hi(w);
+        p[i] = f2_from_bf16x2(w);
       }
-      if constexpr (kRHT) {
-        rht16_unsigned(va);
-        rht16_unsigned(vb);
-      }
+      if constexpr (kRHT) rht16_pairs(p);
       const int64_t gm = m0 + 16 * ch;  // column of the transposed tensor
+      // the block of each column: amax and scale, then both columns scaled
+      // as pairs
+      float ma = 0.0f, mb = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        ma = fmaxf(ma, fabsf(f2_lo(p[i])));
+        mb = fmaxf(mb, fabsf(f2_hi(p[i])));
+      }
+      uint32_t Ea, Eb;
+      float enca, encb;
+      block_scale_tab(ma, s_t, enc_tab[1], Ea, enca);
+      block_scale_tab(mb, s_t, enc_tab[1], Eb, encb);
+      const uint64_t enc2 = f2_pack(__float_as_uint(enca), __float_as_uint(encb));
+      float sa[16], sb[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint64_t v = f2_mul(p[i], enc2);
+        sa[i] = f2_lo(v);
+        sb[i] = f2_hi(v);
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        float* s = h ? sb : sa;
         const int64_t gr = c0 + pc + h;  // row of the transposed tensor
-        uint32_t E;
-        const uint2 o = quantize16<kSR>(h ? vb : va, s_t, enc_tab[1], E, key, ot.stream, (uint64_t)(gr * rows + gm));
-        *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = o;
-        ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)E;
+        if constexpr (kSR) {
+          uint32_t nu[16];
+          sr_nu16(key, ot.stream, (uint64_t)(gr * rows + gm), nu);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) s[i] = e2m1_sr_value(s[i], nu[i]);
+        }
+        *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = make_uint2(e2m1x8_rn(s), e2m1x8_rn(s + 8));
+        ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)(h ? Eb : Ea);
       }
     }
   }
