@@ -19,7 +19,15 @@ computes, written from:
 * Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
   (SC'11), for Philox4x32-10.
 
+Two restatements of the same definitions, pinned by the same kinds of tests
+and equal to each other bit for bit: the numpy modules below (the reference
+used by most parity tests), and a plain C++17 library, ``cxx`` (source
+``cxx/nvfp4_oracle.cpp``, std::thread over the host's cores, compiled with
+-ffp-contract=off), which the full-size parity checks and the benchmark's CPU
+baseline use.
+
 Modules:
+  cxx      ctypes binding of the C++ oracle (same function names)
   formats  E2M1 / E4M3 encode and decode, nibble packing
   philox   Philox4x32-10 counter-based generator
   rht      16x16 random Hadamard transform
@@ -35,3 +43,4 @@ convention; it is pinned only through the GPU GEMM (parity unpinned on CPU).
 """
 
 from . import formats, philox, rht, quant, gemm, linear  # noqa: F401
+# oracle.cxx is imported on demand (it compiles its C++ library on first use)
