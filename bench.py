@@ -190,16 +190,65 @@ def library_gemms(pairs, stream):
     return res
 
 
-def cpu_oracle_step(x_f, w_f, dy_f):
+def cpu_oracle_step(x_f, w_f, dy_f, threads=0):
     """One bounded oracle sample: the whole layer step for a 64-token slice of
-    X and dY (all of W).  Returns (seconds, flops)."""
-    from oracle import linear
+    X and dY (all of W), through the plain C++ oracle on the host's cores.
+    Returns (seconds, flops)."""
+    from oracle import cxx
 
     xs, dys = x_f[:ORACLE_TOKENS], dy_f[:ORACLE_TOKENS]
     t0 = time.perf_counter()
-    f = linear.linear_fwd(xs, w_f, SEED)
-    linear.linear_bwd(dys, f, SEED)
+    f = cxx.linear_fwd(xs, w_f, SEED, threads=threads)
+    cxx.linear_bwd(dys, f, SEED, threads=threads)
     return time.perf_counter() - t0, 6 * ORACLE_TOKENS * K * N
+
+
+def cpu_quantize_full(x_f, w_f, dy_f, threads=0):
+    """The layer step's three quantize passes in full through the plain C++
+    oracle: X [8192, 5120] (amax, amax of the transform along tokens, rowwise
+    RNE, transposed Hadamard RNE), W [20480, 5120] (amax, 16x16 blocks, W and
+    W^T), dY [8192, 20480] (amax, amax of the transform, rowwise SR, transposed
+    Hadamard SR).  Returns {tensor: seconds}."""
+    from oracle import cxx
+
+    out = {}
+    t0 = time.perf_counter()
+    cxx.quantize_1d(x_f, "rne", amax=cxx.tensor_amax(x_f, threads), threads=threads)
+    cxx.quantize_transpose(x_f, "rne", rht_seed=SEED, amax=cxx.amax_rht(x_f, SEED, 0, threads), threads=threads)
+    out["x"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    cxx.quantize_2d(w_f, threads=threads)
+    out["w"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    cxx.quantize_1d(dy_f, "sr", seed=SEED, stream_id=0, amax=cxx.tensor_amax(dy_f, threads), threads=threads)
+    cxx.quantize_transpose(dy_f, "sr", seed=SEED, stream_id=1, rht_seed=SEED,
+                           amax=cxx.amax_rht(dy_f, SEED, 0, threads), threads=threads)
+    out["dy"] = time.perf_counter() - t0
+    return out
+
+
+def cpu_baseline_record(x_f, w_f, dy_f):
+    """The bench line's cpu_baseline: the C++ oracle with one std::thread per
+    host core, timed on the layer step's quantize passes in full and on a
+    64-token slice of the whole layer step (the GEMMs, float64 on the
+    dequantized operands, are the bulk of the oracle's work)."""
+    cores = os.cpu_count()
+    s, flops = cpu_oracle_step(x_f, w_f, dy_f, threads=cores)
+    q = cpu_quantize_full(x_f, w_f, dy_f, threads=cores)
+    elems = {"x": M * K, "w": N * K, "dy": M * N}
+    # algorithmic bytes: BF16 read once per amax pass and once per quantize
+    # pass, 0.5625 B per element per NVFP4 output
+    qbytes = {"x": elems["x"] * (2 * 2 + 2 * 0.5625), "w": elems["w"] * (2 * 2 + 2 * 0.5625),
+              "dy": elems["dy"] * (2 * 2 + 2 * 0.5625)}
+    return {
+        "value": flops / s / 1e12, "unit": "TFLOP/s", "cores": cores, "threads": cores, "kind": "oracle",
+        "sample": "plain C++ oracle (oracle/cxx), one std::thread per core: the layer step on a %d-token "
+                  "slice of X and dY with all of W (%.1f GFLOP, float64 GEMMs), %.2f s" % (ORACLE_TOKENS,
+                                                                                         flops / 1e9, s),
+        "quantize_full": {k: {"s": v, "gbs": qbytes[k] / v / 1e9} for k, v in q.items()},
+        "quantize_full_note": "each tensor's amax and quantize passes of the layer step in full "
+                              "(X 8192x5120, W 20480x5120, dY 8192x20480)",
+    }
 
 
 def run_reference(args, rank, world):
@@ -211,24 +260,26 @@ def run_reference(args, rank, world):
 
     x, w, dy = workloads.mlp_up()
     x_f, w_f, dy_f = (workloads.bf16_to_f32_numpy(t) for t in (x, w, dy))
+    cores = os.cpu_count()
     for _ in range(args.warmup):
-        cpu_oracle_step(x_f, w_f, dy_f)
+        cpu_oracle_step(x_f, w_f, dy_f, threads=cores)
     times = []
     flops = 0
     for _ in range(args.steps):
-        dt, fl = cpu_oracle_step(x_f, w_f, dy_f)
+        dt, fl = cpu_oracle_step(x_f, w_f, dy_f, threads=cores)
         times.append(dt)
         flops = fl
     mean = sum(times) / len(times)
     value = flops / mean / 1e12
-    cores = os.cpu_count()
-    sample = "%d-token slice of the layer step (all of W), %.1f GFLOP per step" % (ORACLE_TOKENS, flops / 1e9)
+    sample = ("plain C++ oracle, one std::thread per core: the layer step on a %d-token slice of X and dY "
+              "with all of W, %.1f GFLOP per step" % (ORACLE_TOKENS, flops / 1e9))
     line = {
         "impl": "reference", "metric": "NVFP4 linear fwd+bwd TFLOPS", "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "sample_tokens": ORACLE_TOKENS},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "threads": cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -409,7 +460,7 @@ def run_gpu(args, rank, world, local):
     dy_elems = M * N
     q_bytes = dy_elems * (2 + 2 + 2 * 0.5625)
     q_ms = float(np.mean(part[:, 3]))
-    cpu_s, cpu_flops = cpu_oracle_step(*(workloads.bf16_to_f32_numpy(t) for t in (x_h, w_h, dy_h)))
+    cpu = cpu_baseline_record(*(workloads.bf16_to_f32_numpy(t) for t in (x_h, w_h, dy_h)))
     value = whole_job_tflops(ms_per_step, world)
     line = {
         "metric": "NVFP4 linear fwd+bwd TFLOPS", "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -438,10 +489,7 @@ def run_gpu(args, rank, world, local):
         "context": dict(context, note="library GEMMs of the same shapes for comparison; not this "
                                       "library's path (out = A B^T: Fprop X W^T, Dgrad dY W, Wgrad dY^T X)"),
         "clocks": clk,
-        "cpu_baseline": {"value": cpu_flops / cpu_s / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-                         "kind": "oracle",
-                         "sample": "%d-token slice of the layer step (all of W); numpy elementwise on one "
-                                   "thread, float64 BLAS GEMM on the host's cores" % ORACLE_TOKENS},
+        "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
     return 0

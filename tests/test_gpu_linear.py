@@ -104,3 +104,28 @@ def test_layer_full_size_sampled(layer):
     assert rel_fro(dx[rm].float().cpu().numpy(), formats.float64_to_bf16_rne(dxr)) <= TOL
     dwr = gemm.gemm_ref(dytq["codes"], dytq["scales"], dytq["ts"], xtq["codes"], xtq["scales"], xtq["ts"])
     assert rel_fro(dw[rn].float().cpu().numpy(), formats.float64_to_bf16_rne(dwr)) <= TOL
+
+
+def test_layer_full_size_every_operand_cxx_oracle():
+    """The benchmark's layer (MLP up-projection, M=8192, K=5120, N=20480) with
+    every element of all six quantized operands -- X and X^T (Hadamard, RNE),
+    W and W^T (16x16 blocks), dY (stochastic) and dY^T (Hadamard, stochastic)
+    -- codes, block scales, amax and tensor scale compared bit for bit with the
+    plain C++ oracle, which runs the whole tensors on the host's cores."""
+    from oracle import cxx
+
+    x, w, dy = workloads.mlp_up()
+    M, K = x.shape
+    N = w.shape[0]
+    seed = 2
+    _, _, _, v = run_layer(x, w, dy, seed)
+    xf, wf, dyf = f32(x), f32(w), f32(dy)
+    assert_q_equal(v["xq"], cxx.quantize_1d(xf, "rne"), what="xq")
+    assert_q_equal(v["xtq"], cxx.quantize_transpose(xf, "rne", rht_seed=seed), what="xtq")
+    wq = cxx.quantize_2d(wf)
+    assert_q_equal(v["wq"], dict(codes=wq["codes"], scales=wq["scales"], amax=wq["amax"], ts=wq["ts"]), what="wq")
+    assert_q_equal(v["wtq"], dict(codes=wq["codes_t"], scales=wq["scales_t"], amax=wq["amax"], ts=wq["ts"]),
+                   what="wtq")
+    assert_q_equal(v["dyq"], cxx.quantize_1d(dyf, "sr", seed=seed, stream_id=linear.SR_STREAM_DY), what="dyq")
+    assert_q_equal(v["dytq"], cxx.quantize_transpose(dyf, "sr", seed=seed, stream_id=linear.SR_STREAM_DYT,
+                                                     rht_seed=seed), what="dytq")
