@@ -760,6 +760,31 @@ def run_next(args, rank, world, local):
     return 0
 
 
+def run_profile_once(local):
+    """One layer step through the public API on the benchmark's inputs (about
+    1.6 GB on the device), for a profiler to capture single launches of it.
+    The side stream of nvfp4_linear_fwd is joined before the GEMM, so the
+    launch order is X amax, X quantize (or W's two on the side stream first),
+    Fprop, dY amax, dY quantize, Dgrad, Wgrad."""
+    import torch
+
+    from nvfp4_bit_numerics_gb300 import binding as B, build as nbuild, workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    nbuild.build()
+    B.load_library()
+    x, w, dy = (t.to(dev) for t in workloads.mlp_up())
+    ws = B.linear_workspace(M, K, N, device=dev)
+    B.nvfp4_linear_fwd(x, w, SEED, ws)
+    B.nvfp4_linear_bwd(dy, K, SEED, ws)
+    st = B.nvfp4_get_status()
+    if st != B.NVFP4_OK:
+        raise RuntimeError("device status %d" % st)
+    print(json.dumps({"profile_once": WORKLOAD, "launches": int(B.nvfp4_kernel_launch_count())}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -770,6 +795,10 @@ def main():
                     help="instead of the benchmark line, one line per further configured shape")
     ap.add_argument("--quant-sweep", action="store_true",
                     help="instead of the benchmark line, only the quantize-only sweep of --sweep")
+    ap.add_argument("--profile-once", action="store_true",
+                    help="for profiler captures: the layer step once (9 kernel launches: X amax, X quantize, "
+                         "W amax, W 2D quantize, Fprop GEMM, dY amax, dY quantize, Dgrad GEMM, Wgrad GEMM) "
+                         "on the benchmark's inputs, nothing else timed or launched after it")
     ap.add_argument("--next", action="store_true",
                     help="instead of the benchmark line, the further paths: GEMM-epilogue amax, the MXFP4 "
                          "layer step, a BF16 layer step")
@@ -779,6 +808,8 @@ def main():
     rank, world, local = dist_info()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.profile_once:
+        return run_profile_once(local)
     if args.sweep:
         return run_sweep(args, rank, world, local)
     if args.next:
