@@ -493,8 +493,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //               signals the even CTA's `full` barrier, which the even CTA's
 //               producer armed for both CTAs' bytes.
 //   warp 1      even CTA: the MMA warp.  The whole warp runs the loop in step
-//               (so descriptors and addresses stay warp-uniform) and one
-//               elected lane issues, per stage: 12 tcgen05.cp.32x128b.warpx4
+//               (so descriptors and addresses stay warp-uniform; a stage's
+//               barrier is one test by all lanes, lane 0 waiting only when it
+//               is not complete yet) and one lane, elected once, issues, per
+//               stage: 12 tcgen05.cp.32x128b.warpx4
 //               copies of the scale tiles from shared memory into the stage's
 //               tensor-memory scale region (replicated into the four lane
 //               quadrants, the layout the MMA reads), the 4 MMAs
@@ -502,8 +504,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //               commit that frees the stage in both CTAs.  Copies and MMAs
 //               issued by one thread execute in order, so the copies of a
 //               stage land before its MMAs read them.
-//   warps 2-9   epilogue (both CTAs) for the CTA's 128 rows; they release
-//               the accumulator with a remote arrive on the even CTA, then
+//   warps 2-9   epilogue (both CTAs) for the CTA's 128 rows; each lane
+//               reads its row's 128 accumulator columns with one wait and
+//               the warp releases the accumulator at once (a remote arrive
+//               on the even CTA for the odd CTA), then
 //               write BF16 output as 32-row x 16-column boxes staged in a
 //               1 KB shared-memory buffer per warp and sent with bulk tensor
 //               stores.  Optionally each lane also takes the max |D| of its
@@ -732,12 +736,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       if (lane == 0) r = mbar_wait(bar, parity, abort, p.status) ? 1 : 0;
       return __shfl_sync(0xFFFFFFFFu, r, 0) != 0;
     };
+    // per stage: every lane tests the barrier (one instruction, the same
+    // answer for all); only when it is not complete yet does lane 0 wait
+    auto stage_wait = [&](uint32_t bar, uint32_t parity) {
+      if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+      return warp_wait(bar, parity);
+    };
     // one instantiation per operand format: the issue path carries no
     // format test
     auto issue = [&](auto mx_tag) {
       constexpr bool kMX = decltype(mx_tag)::value;
       const uint32_t idesc = idesc_block_scaled(256, kPairBN, kMX);
       const uint32_t tmem_u = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+      // the lane that issues every copy, MMA and commit of this warp
+      const bool leader = elect_one();
       // descriptors of stage 0; stage s adds s * kPairStageBytes
       const uint64_t da0 = desc_sw128(base), db0 = desc_sw128(base + kPairABytes);
       const uint64_t dsf0 = desc_sf_tile(base + kPairABytes + kPairBBytes);
@@ -750,12 +762,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         if (!warp_wait(tmem_empty, acc_phase ^ 1u)) break;
         tc_fence_after();
         for (int ks = 0; ks < k_stages; ++ks) {
-          if (!warp_wait(full_bar(stage), phase)) { ok = false; break; }
+          if (!stage_wait(full_bar(stage), phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t soff = (uint64_t)stage * kStageDesc;
           const uint64_t da = da0 + soff, db = db0 + soff, dsf = dsf0 + soff;
           const uint32_t sfa = tmem_u + (uint32_t)(kPairBN + stage * kPairSfCols), sfb = sfa + 16;
-          if (elect_one()) {
+          if (leader) {
             // scale tiles: A tile j -> columns 4j; B tile (j, h) -> 16 + 8j + 4h
 #pragma unroll
             for (int j = 0; j < 4; ++j) tc_cp_sf_pair(sfa + 4 * j, dsf + j * kTileDesc);
@@ -775,11 +787,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             }
             tc_commit_pair_multicast(empty_bar(stage));
           }
-          __syncwarp();
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        if (elect_one()) tc_commit_pair_multicast(tmem_full);
+        if (leader) tc_commit_pair_multicast(tmem_full);
         __syncwarp();
         acc_phase ^= 1u;
       }
@@ -823,88 +834,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(half * kCols);
       const int64_t row = (int64_t)mb * 256 + (int64_t)rank * 128 + 32 * q + lane;
       const int64_t col0 = (int64_t)nb * kPairBN + half * kCols;
-      uint32_t packed[kCols / 2];
-      uint32_t m32 = 0;  // FP32 output: max magnitude bits
+      // all 128 accumulator columns of this lane's row into registers with one
+      // wait; the accumulator goes back to the MMA warp at once, and the next
+      // tile's MMAs run while this tile is scaled, rounded and stored
+      uint32_t v[kCols];
 #pragma unroll
-      for (int c = 0; c < kCols / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(taddr + 32 * c, v);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (!p.d_f32) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            packed[16 * c + i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[2 * i])),
-                                             __fmul_rn(alpha, __uint_as_float(v[2 * i + 1])));
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0 + 32 * c);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 o = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
-                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
-                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
-                                       __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
-            dst[i] = o;
-            m32 = max(m32, max(max(o.x & 0x7FFFFFFFu, o.y & 0x7FFFFFFFu), max(o.z & 0x7FFFFFFFu, o.w & 0x7FFFFFFFu)));
-          }
-        }
-      }
+      for (int c = 0; c < kCols / 32; ++c) tmem_ld32(taddr + 32 * c, v + 32 * c);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_leader(tmem_empty, rank);
       acc_phase ^= 1u;
-      if (p.tma_store) {
-        // 16-column chunks through this warp's 1 KB buffer: 32 rows of 32 B,
-        // 32-byte swizzle (16-byte half h of row r at h ^ bit 2 of r), one
-        // bulk tensor store per chunk; the buffer is rewritten once the
-        // previous store has read it.
+      if (p.d_f32) {
+        uint32_t m32 = 0;  // max magnitude bits
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0);
+#pragma unroll
+        for (int i = 0; i < kCols / 4; ++i) {
+          const uint4 o = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
+                                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
+                                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
+                                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+          dst[i] = o;
+          m32 = max(m32, max(max(o.x & 0x7FFFFFFFu, o.y & 0x7FFFFFFFu), max(o.z & 0x7FFFFFFFu, o.w & 0x7FFFFFFFu)));
+        }
+        if (p.amax_out) amax_bits_to_global(m32, p.amax_out);
+      } else {
+        // 16-column chunks, each one 1x16 block of the row: scaled and
+        // rounded to BF16, then (as asked) folded into the output amax,
+        // quantized to NVFP4, and sent through this warp's 1 KB buffer (32
+        // rows of 32 B, 32-byte swizzle: 16-byte half h of row r at h ^ bit 2
+        // of r) with one bulk tensor store; the buffer is rewritten once the
+        // previous store has read it
         const uint32_t buf = epi_base + (uint32_t)(warp - kPairFirstEpiWarp) * kPairEpiBufBytes;
         const uint32_t sw = (uint32_t)((lane >> 2) & 1);
+        uint32_t m2 = 0;               // max BF16 magnitude bits of both halves
+        uint32_t sc[2] = {0u, 0u};     // quantized output: 8 block scales
+        uint32_t qw[4] = {0u, 0u, 0u, 0u};
+        uint4* cdst = p.q_codes ? reinterpret_cast<uint4*>(p.q_codes + row * (p.N >> 1) + (col0 >> 1)) : nullptr;
 #pragma unroll
         for (int j = 0; j < kCols / 16; ++j) {
-          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          __syncwarp();
+          uint32_t pk[8];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t a = buf + (uint32_t)lane * 32u + (((uint32_t)h ^ sw) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(packed[8 * j + 4 * h]),
-                         "r"(packed[8 * j + 4 * h + 1]), "r"(packed[8 * j + 4 * h + 2]), "r"(packed[8 * j + 4 * h + 3])
-                         : "memory");
+          for (int i = 0; i < 8; ++i)
+            pk[i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[16 * j + 2 * i])),
+                                __fmul_rn(alpha, __uint_as_float(v[16 * j + 2 * i + 1])));
+          if (p.amax_out) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, pk[i] & 0x7FFF7FFFu);
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) tma_store_2d(&tmap_d, (int)col0 + 16 * j, (int)(row - lane), buf);
-        }
-      }
-      if (p.amax_out) {
-        if (!p.d_f32) amax_bf16_words<kCols / 2>(packed, p.amax_out);
-        else amax_bits_to_global(m32, p.amax_out);
-      }
-      if (p.q_codes) {
-        // this lane's row, 128 columns = 8 blocks of 16 BF16 values, each
-        // quantized as the rowwise RNE quantizer would quantize the stored
-        // BF16 output: 64 code bytes and two 4-scale words
-        uint32_t sc[2] = {0u, 0u};
-        uint4* cdst = reinterpret_cast<uint4*>(p.q_codes + row * (p.N >> 1) + (col0 >> 1));
-#pragma unroll
-        for (int b = 0; b < kCols / 16; b += 2) {
-          uint2 o[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[16];
+          if (p.q_codes) {
+            // as the rowwise RNE quantizer would quantize the stored BF16 output
+            float f[16];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              v[2 * i] = bf16lo(packed[8 * (b + h) + i]);
-              v[2 * i + 1] = bf16hi(packed[8 * (b + h) + i]);
+              f[2 * i] = bf16lo(pk[i]);
+              f[2 * i + 1] = bf16hi(pk[i]);
             }
             uint32_t E;
-            o[h] = quantize16_rne(v, q_senc, E);
-            sc[(b + h) >> 2] |= E << (8 * ((b + h) & 3));
+            const uint2 o = quantize16_rne(f, q_senc, E);
+            sc[j >> 2] |= E << (8 * (j & 3));
+            qw[2 * (j & 1)] = o.x;
+            qw[2 * (j & 1) + 1] = o.y;
+            if (j & 1) cdst[j >> 1] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
           }
-          cdst[b >> 1] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+          if (p.tma_store) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t a = buf + (uint32_t)lane * 32u + (((uint32_t)h ^ sw) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * h]), "r"(pk[4 * h + 1]),
+                           "r"(pk[4 * h + 2]), "r"(pk[4 * h + 3])
+                           : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&tmap_d, (int)col0 + 16 * j, (int)(row - lane), buf);
+          }
         }
-        const int64_t n_kb = p.N >> 4, kb0 = col0 >> 4;
-        *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0, n_kb)) = sc[0];
-        *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0 + 4, n_kb)) = sc[1];
+        if (p.amax_out) amax_bits_to_global(max(m2 & 0xFFFFu, m2 >> 16) << 16, p.amax_out);
+        if (p.q_codes) {
+          const int64_t n_kb = p.N >> 4, kb0 = col0 >> 4;
+          *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0, n_kb)) = sc[0];
+          *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0 + 4, n_kb)) = sc[1];
+        }
       }
     }
     // the output is in global memory (and the buffers free) before exit
