@@ -3,7 +3,7 @@
 // of tile_ring.cuh, stochastic rounding with per-thread loads), the 128x64
 // tile kernel that writes the rowwise and/or the transposed (token-major,
 // Hadamard-transformed) operand from one read, and the 16x16 2D weight
-// quantization that writes W and W^T.
+// quantization (on the tile ring) that writes W and W^T.
 //
 // Method: "Pretraining Large Language Models with NVFP4" (gist.science
 // summary), Resumo técnico §2 Metodologia: two-level NVFP4 scaling ("Escala
@@ -357,7 +357,7 @@ struct TileOut {
   uint32_t stream;
 };
 
-constexpr int kTile = 64;       // 2D kernel tile, and the column width of the tile kernel
+constexpr int kTile = 64;       // column width of the tile kernel
 constexpr int kTileRows = 128;  // rows (tokens) per tile of the tile kernel
 constexpr int kTilePitch = 72;  // uint16 per smem row: 144 B, conflict-free 16 B row reads
 
@@ -477,75 +477,55 @@ __global__ void __launch_bounds__(kThreads, 3) quant_tile_kernel(const uint16_t*
 }
 
 // ---------------------------------------------------------------------------
-// 2D weight quantization: persistent over 64 x 128 tiles (4 x 8 blocks of
-// 16 x 16) staged in shared memory.
-//  - block pass: thread (br, bc, rp) holds rows rp and rp + 8 of block (br, bc);
-//    the block amax is a shuffle over the 8 threads of the block; it encodes
-//    its two rows (W codes, K-major).
-//  - column pass: thread (br, column pair) encodes the 16 x 2 column slice of
-//    its block with the same block scale (W^T codes, N-major).  Encoding an
-//    element twice gives the same code, so W^T is exactly W transposed.  The
-//    W^T codes of the tile (128 rows of 32 bytes) are collected in shared
-//    memory and written as one 16-byte store per thread, whole sectors per
-//    row, instead of 8-byte pieces of 64 rows per warp instruction.
-//  - scales: one 32-bit store per 4 blocks of a row of W and of W^T.
+// 2D weight quantization on the TMA tile ring (tile_ring.cuh): 128 x 64 tiles
+// (8 x 4 blocks of 16 x 16) stream into a shared-memory ring while the 8
+// consumer warps encode them.
+//  - block pass: the 8 threads (consecutive lanes) of block (br, bc) hold
+//    rows p and p + 8 of it; the block amax is a shuffle over the 8; each
+//    thread encodes its two rows (W codes, K-major, 8 bytes per row).
+//  - scales: one 32-bit word per row of W (its 4 blocks of the tile) and two
+//    per row of W^T (its 8 blocks), from the tile's 32 block scales.
+//  - column pass: thread (cp, brr) encodes the 16 x 2 slice (columns 2 cp,
+//    2 cp + 1 of block row brr) with the block's scale, reading one 32-bit
+//    word per row (a warp reads one whole 128-byte row: no bank conflicts);
+//    encoding an element twice gives the same code, so W^T is exactly W
+//    transposed.  The W^T codes of the tile (64 rows of 64 bytes) are
+//    collected in shared memory and written as one 16-byte store per thread,
+//    whole sectors per row.
+// Two barriers of the 256 consumer threads per tile (named barrier 1; the
+// ring's producer warp does not take part).
 // ---------------------------------------------------------------------------
-constexpr int k2dRows = 64, k2dCols = 128;
-constexpr int k2dPitch = 136;  // uint16 per smem row: 272 B
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kThreads, 3) quant_2d_kernel(const uint16_t* __restrict__ w, int64_t rows,
-                                                            int64_t cols, const float* amax, TileOut ow,
-                                                            TileOut owt, int has_t, uint32_t* status) {
-  __shared__ __align__(16) uint16_t tile[k2dRows * k2dPitch];
-  __shared__ __align__(16) uint2 tbuf[4][k2dCols];  // W^T codes: [block row][W^T row of the tile]
-  __shared__ float s_enc[4][8];
-  __shared__ uint32_t s_E[4][8];
+__global__ void __launch_bounds__(kRingThreads, 3)
+    quant_2d_ring_kernel(const __grid_constant__ CUtensorMap wmap, int64_t rows, int64_t cols, const float* amax,
+                         TileOut ow, TileOut owt, int has_t, uint32_t* status, int debug_stall) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float s_enc[8][4];
+  __shared__ uint32_t s_E[8][4];
+  __shared__ __align__(16) uint2 tbuf[64][8];  // W^T codes: [W^T row of the tile][block row]
   const int t = threadIdx.x;
   const float s_tensor = tensor_prologue(amax, ow.ts, status);
   if (has_t && blockIdx.x == 0 && t == 0) *owt.ts = tensor_decode_scale(s_tensor);
-  const int64_t tiles_c = (cols + k2dCols - 1) / k2dCols;  // cols % 64 == 0
-  const int64_t n_tiles = (rows / k2dRows) * tiles_c;
-  const int br = t >> 6, bc = (t >> 3) & 7, rp = t & 7;
-
-  // the next tile's loads are issued before the current tile is processed
-  uint4 q[4];
-  const uint32_t tiles_c32 = (uint32_t)tiles_c;  // tile counts < 2^32 (launcher): 32-bit index math
-  auto load_tile = [&](uint32_t tl) {
-    const uint32_t tm = tl / tiles_c32, tc = tl - tm * tiles_c32;
-    const int64_t r0 = (int64_t)tm * k2dRows, c0 = (int64_t)tc * k2dCols;
-    const int valid_cols = cols - c0 < k2dCols ? (int)(cols - c0) : k2dCols;
+  // block pass role
+  const int blk = t >> 3, p = t & 7, br = blk >> 2, bc = blk & 3;
+  uint32_t roff[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int v = t + k * kThreads;  // 64 rows x 16 vectors
-      const int row = v >> 4, cv = v & 15;
-      q[k] = cv * 8 < valid_cols ? ldg_nc_v4(w + (r0 + row) * cols + c0 + cv * 8) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  if (blockIdx.x < n_tiles) load_tile(blockIdx.x);
-  for (uint32_t tl = blockIdx.x; tl < (uint32_t)n_tiles; tl += gridDim.x) {
-    const uint32_t tm = tl / tiles_c32, tc = tl - tm * tiles_c32;
-    const int64_t r0 = (int64_t)tm * k2dRows, c0 = (int64_t)tc * k2dCols;
-    const int valid_cols = cols - c0 < k2dCols ? (int)(cols - c0) : k2dCols;  // 64 or 128
-    __syncthreads();  // the previous tile's readers are done
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int v = t + k * kThreads;
-      *reinterpret_cast<uint4*>(&tile[(v >> 4) * k2dPitch + (v & 15) * 8]) = q[k];
-    }
-    __syncthreads();
-    if (tl + gridDim.x < n_tiles) load_tile(tl + gridDim.x);
-
+  for (int h = 0; h < 2; ++h) {
+    roff[2 * h] = ring_chunk(16 * br + p + 8 * h, 2 * bc);
+    roff[2 * h + 1] = ring_chunk(16 * br + p + 8 * h, 2 * bc + 1);
+  }
+  // column pass role: column pair cp, block row brr; row i of the block at
+  // coff + 128 i (16 rows of one block share (i % 8) only through the
+  // swizzle, so the offset of each row is recomputed from a base)
+  const int cp = t & 31, brr = t >> 5;
+  const int64_t n_kb_w = cols >> 4, n_kb_t = rows >> 4;
+  tile_ring(&wmap, rows, cols, status, debug_stall, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
     // ---- block pass: amax, scale, W codes
-    const bool col_ok = bc * 16 < valid_cols;
+    const bool row_ok = 16 * br < valid;
     float v[32];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4* sp = reinterpret_cast<const uint4*>(&tile[(16 * br + rp + 8 * h) * k2dPitch + bc * 16]);
-      unpack8(sp[0], v + 16 * h);
-      unpack8(sp[1], v + 16 * h + 8);
-    }
-    // block amax as a float max of |v| (the tensor's amax pass reports
-    // non-finite input)
+    for (int j = 0; j < 4; ++j) unpack8(lds128(tile + roff[j]), v + 8 * j);
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
@@ -555,64 +535,68 @@ __global__ void __launch_bounds__(kThreads, 3) quant_2d_kernel(const uint16_t* _
     uint32_t E;
     float enc;
     block_scale(m, s_tensor, E, enc);
-    if (rp == 0) {
+    if (p == 0) {
       s_E[br][bc] = E;
       s_enc[br][bc] = enc;
     }
-    if (col_ok) {
+    if (row_ok) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float sv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) sv[i] = __fmul_rn(v[16 * h + i], enc);
-        const int64_t gr = r0 + 16 * br + rp + 8 * h, gc = c0 + bc * 16;
+        const int64_t gr = m0 + 16 * br + p + 8 * h, gc = c0 + 16 * bc;
         *reinterpret_cast<uint2*>(ow.codes + gr * (cols >> 1) + (gc >> 1)) =
             make_uint2(e2m1x8_rn(sv), e2m1x8_rn(sv + 8));
       }
     }
-    __syncthreads();
-
-    // ---- scales: W rows (4 blocks per store), W^T rows (4 block rows per store)
+    consumer_sync();
+    // ---- scales: W rows (4 blocks of the tile per word), W^T rows (4 block
+    // rows per word)
     if (t < 128) {
-      const int row = t >> 1, g = t & 1;
-      if (g * 64 < valid_cols) {
-        const int b = row >> 4;
-        const uint32_t w4 = s_E[b][4 * g] | (s_E[b][4 * g + 1] << 8) | (s_E[b][4 * g + 2] << 16) |
-                            (s_E[b][4 * g + 3] << 24);
-        *reinterpret_cast<uint32_t*>(ow.scales + sf_offset(ow.layout, r0 + row, (c0 >> 4) + 4 * g, cols >> 4)) =
-            w4;
+      if (t < valid) {
+        const int b = t >> 4;
+        const uint32_t w4 = s_E[b][0] | (s_E[b][1] << 8) | (s_E[b][2] << 16) | (s_E[b][3] << 24);
+        *reinterpret_cast<uint32_t*>(ow.scales + sf_offset(ow.layout, m0 + t, c0 >> 4, n_kb_w)) = w4;
       }
-    } else if (has_t && t - 128 < valid_cols) {
-      const int k = t - 128, b = k >> 4;
-      const uint32_t w4 = s_E[0][b] | (s_E[1][b] << 8) | (s_E[2][b] << 16) | (s_E[3][b] << 24);
-      *reinterpret_cast<uint32_t*>(owt.scales + sf_offset(owt.layout, c0 + k, r0 >> 4, rows >> 4)) = w4;
+    } else if (has_t) {
+      const int u = t - 128, k = u >> 1, g = u & 1;
+      if (64 * g < valid) {
+        const int b = k >> 4;
+        const uint32_t w4 = s_E[4 * g][b] | (s_E[4 * g + 1][b] << 8) | (s_E[4 * g + 2][b] << 16) |
+                            (s_E[4 * g + 3][b] << 24);
+        *reinterpret_cast<uint32_t*>(owt.scales + sf_offset(owt.layout, c0 + k, (m0 >> 4) + 4 * g, n_kb_t)) = w4;
+      }
     }
-    if (!has_t) continue;
-
-    // ---- column pass: W^T codes, collected per tile, then whole rows
-    {
-      const int cp = t & 63, bcc = cp >> 3;
-      if (bcc * 16 < valid_cols) {
-        float va[16], vb[16];
+    if (!has_t) {
+      consumer_sync();  // s_E / s_enc are rewritten by the next tile
+      return;
+    }
+    // ---- column pass: W^T codes of this block row
+    if (16 * brr < valid) {
+      const float e = s_enc[brr][cp >> 3];
+      float va[16], vb[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t wd = *reinterpret_cast<const uint32_t*>(&tile[(16 * br + i) * k2dPitch + 2 * cp]);
-          va[i] = __fmul_rn(bf16lo(wd), s_enc[br][bcc]);
-          vb[i] = __fmul_rn(bf16hi(wd), s_enc[br][bcc]);
-        }
-        tbuf[br][2 * cp] = make_uint2(e2m1x8_rn(va), e2m1x8_rn(va + 8));
-        tbuf[br][2 * cp + 1] = make_uint2(e2m1x8_rn(vb), e2m1x8_rn(vb + 8));
+      for (int i = 0; i < 16; ++i) {
+        const int r = 16 * brr + i;
+        const uint32_t wd = lds32(tile + ring_chunk(r, cp >> 2) + ((cp & 3) << 2));
+        va[i] = __fmul_rn(bf16lo(wd), e);
+        vb[i] = __fmul_rn(bf16hi(wd), e);
       }
-      __syncthreads();
-      // thread t: W^T row t / 2 of the tile, 16 bytes (block rows 2h, 2h + 1)
-      const int lr = t >> 1, h = t & 1;
-      if (lr < valid_cols) {
-        const uint2 a = tbuf[2 * h][lr], b = tbuf[2 * h + 1][lr];
-        *reinterpret_cast<uint4*>(owt.codes + (c0 + lr) * (rows >> 1) + (r0 >> 1) + 16 * h) =
+      tbuf[2 * cp][brr] = make_uint2(e2m1x8_rn(va), e2m1x8_rn(va + 8));
+      tbuf[2 * cp + 1][brr] = make_uint2(e2m1x8_rn(vb), e2m1x8_rn(vb + 8));
+    }
+    consumer_sync();
+    // thread t: W^T row t / 4 of the tile, 16 bytes (block rows 2q, 2q + 1)
+    {
+      const int k = t >> 2, q = t & 3;
+      if (32 * q < valid) {
+        const uint2 a = tbuf[k][2 * q], b = tbuf[k][2 * q + 1];
+        *reinterpret_cast<uint4*>(owt.codes + (c0 + k) * (rows >> 1) + (m0 >> 1) + 16 * q) =
             make_uint4(a.x, a.y, b.x, b.y);
       }
     }
-  }
+  });
 }
 
 }  // namespace
@@ -740,12 +724,21 @@ cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvf
   TileOut ow{out.codes, out.scales, amax, out.tensor_scale, out.scale_layout, 0};
   TileOut owt{};
   if (out_t) owt = TileOut{out_t->codes, out_t->scales, amax, out_t->tensor_scale, out_t->scale_layout, 0};
-  const int64_t tiles = (rows / k2dRows) * ((cols + k2dCols - 1) / k2dCols);
-  if (tiles >= kMaxUnits) return cudaErrorInvalidValue;
-  const int64_t cap = (int64_t)sm_count() * 8;
-  const unsigned grid = (unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
-  quant_2d_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(w), rows, cols, amax, ow, owt,
-                                            out_t ? 1 : 0, device_status_ptr());
+  const int64_t tiles = ring_tiles(rows, cols);
+  if (tiles >= kRingMaxTiles) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  if (!make_ring_map(&map, w, rows, cols)) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(quant_2d_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  quant_2d_ring_kernel<<<ring_grid(tiles, 3), kRingThreads, kRingSmemBytes, s>>>(
+      map, rows, cols, amax, ow, owt, out_t ? 1 : 0, device_status_ptr(), take_ring_debug_stall());
   count_launch();
   return cudaGetLastError();
 }
