@@ -121,33 +121,88 @@ __device__ __forceinline__ uint32_t e2m1x8_rn(const float* v) {
   return r;
 }
 
-// Stochastic rounding of one value with a 16-bit uniform u: with lo the
-// lower grid neighbour of |v| and step the grid spacing there,
-// frac = (|v| - lo) / step, and the value rounds up iff u < frac * 2^16.
-// The result is the rounded grid value with the sign of v, or for |v| > 6 a
-// value at least 6, which the saturating conversion to E2M1 turns into 6
-// (code 7).  The caller passes nu = 2^22 - 1 - 64 u.
-//   |v| in [1, 8):  lo keeps the exponent and the top mantissa bit of |v|,
-//                   and frac * 2^22 is the integer m of the lower 22 mantissa
-//                   bits.  64 u < m  <=>  m + nu >= 2^22: adding nu to the
-//                   bits carries into bit 22 exactly when the value rounds
-//                   up, and clearing the lower 22 bits leaves lo or its upper
-//                   neighbour (a carry out of the mantissa steps the
-//                   exponent, which is the next grid point as well).
-//   |v| in [0, 1):  the grid 0, .5, 1 is 1, 1.5, 2 shifted by one.  x =
-//                   RU(|v| + 1) has lower 22 mantissa bits ceil(frac * 2^22),
-//                   and for an integer n, n < y <=> n < ceil(y), so the same
-//                   carry test on x decides exactly; 1 is subtracted after
-//                   (exact).  The shift, 1 below 1 and 0 from 1 up, is one
-//                   saturating FMA: sat(2^126 (1 - |v|)).
-//   |v| >= 8:       the truncated value stays >= 8 and saturates to 6.
-// Non-finite inputs (which the amax pass reports) give unspecified codes.
-__device__ __forceinline__ float e2m1_sr_value(float v, uint32_t nu) {
-  const float av = fabsf(v);
-  const float off = __saturatef(__fmaf_rn(-av, 0x1p126f, 0x1p126f));
-  const float x = __fadd_ru(av, off);
-  const float r = __uint_as_float((__float_as_uint(x) + nu) & 0xFFC00000u);
-  return __uint_as_float(__float_as_uint(__fsub_rn(r, off)) | (__float_as_uint(v) & 0x80000000u));
+// ---------------------------------------------------------------------------
+// Packed float pairs: two IEEE float32 values in one 64-bit register pair,
+// operated on by the paired instructions (add/sub/mul/fma .rn.f32x2), which
+// round each half exactly as the scalar instruction would.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t p) { return __uint_as_float((uint32_t)p); }
+__device__ __forceinline__ float f2_hi(uint64_t p) { return __uint_as_float((uint32_t)(p >> 32)); }
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// a * b + c in one rounding per half
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// The two BF16 values of a 32-bit word as a float pair (element 0 low).
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) { return f2_pack(w << 16, w & 0xFFFF0000u); }
+
+// max(|a|, |b|) of each BF16 half (the sign of the result is not used).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Stochastic rounding of 16 values to E2M1 codes (8 bytes).  The rule: with
+// lo the lower grid neighbour of |s| (grid 0 .5 1 1.5 2 3 4 6) and step the
+// grid spacing there, frac = (|s| - lo) / step, and |s| rounds up iff
+// u < frac * 2^16 (u the element's 16-bit uniform); the sign is kept and
+// values above 6 give 6.  The caller passes nu = 2^22 - 1 - 64 u.
+// y = RU(|s| * 2^-126) maps the grid onto float bit patterns: .5, 1, 1.5,
+// 2, 3, 4, 6 become 1, 2, 3, 4, 5, 6, 7 times 2^22 (the grid below 1 lands in
+// the subnormals, whose spacing is uniform like the grid's there), so in
+// every binade the lower 22 bits of y are m = ceil(frac * 2^22), exact above
+// 1 and rounded up by RU below.  For an integer n, n < x <=> n < ceil(x), so
+// 64 u < frac * 2^22 <=> 64 u < m <=> m + nu >= 2^22: adding nu carries into
+// bit 22 exactly when the value rounds up, and clearing the lower 22 bits
+// leaves the lower or the upper neighbour (a carry out of the mantissa steps
+// the exponent, the next grid point as well).  Scaling back by 2^126 is
+// exact; the saturating conversion turns results above 6 into 6.  Non-finite
+// inputs (which the amax pass reports) give unspecified codes.
+__device__ __forceinline__ float mul_ru_2m126(float a) {
+  float y;
+  asm("mul.rp.f32 %0, %1, 0f00800000;" : "=f"(y) : "f"(a));
+  return y;
+}
+__device__ __forceinline__ uint2 sr_codes16(const float* s, const uint32_t* nu) {
+  const uint64_t k126 = f2_pack(0x7E800000u, 0x7E800000u);
+  float z[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float a = s[2 * j], b = s[2 * j + 1];
+    const uint32_t ra = (__float_as_uint(mul_ru_2m126(fabsf(a))) + nu[2 * j]) & 0xFFC00000u;
+    const uint32_t rb = (__float_as_uint(mul_ru_2m126(fabsf(b))) + nu[2 * j + 1]) & 0xFFC00000u;
+    const uint64_t zz = f2_mul(f2_pack(ra, rb), k126);
+    z[2 * j] = __uint_as_float((uint32_t)zz | (__float_as_uint(a) & 0x80000000u));
+    z[2 * j + 1] = __uint_as_float((uint32_t)(zz >> 32) | (__float_as_uint(b) & 0x80000000u));
+  }
+  return make_uint2(e2m1x8_rn(z), e2m1x8_rn(z + 8));
 }
 
 // ---------------------------------------------------------------------------
@@ -294,14 +349,9 @@ __device__ __forceinline__ uint2 quantize16(const float* v, float s_enc, const f
   if constexpr (kSR) {
     uint32_t nu[16];
     sr_nu16(key, stream, e0, nu);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = e2m1_sr_value(s[i], nu[i]);
+    return sr_codes16(s, nu);
   }
-  // RNE here, or the exact conversion of grid values after SR
-  uint2 out;
-  out.x = e2m1x8_rn(s);
-  out.y = e2m1x8_rn(s + 8);
-  return out;
+  return make_uint2(e2m1x8_rn(s), e2m1x8_rn(s + 8));
 }
 
 // The same block with round-to-nearest-even and enc computed by its division

@@ -249,49 +249,14 @@ __global__ void __launch_bounds__(kRingThreads, 3)
   });
 }
 
-// ---------------------------------------------------------------------------
-// Packed float pairs: two IEEE float32 values in one 64-bit register pair,
-// operated on by the paired instructions (add/sub/mul/fma .rn.f32x2), which
-// round each half exactly as the scalar instruction would.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
-  return r;
-}
-__device__ __forceinline__ float f2_lo(uint64_t p) { return __uint_as_float((uint32_t)p); }
-__device__ __forceinline__ float f2_hi(uint64_t p) { return __uint_as_float((uint32_t)(p >> 32)); }
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-// a * b + c in one rounding per half
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-// The two BF16 values of a 32-bit word as a float pair (element 0 low).
-__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) { return f2_pack(w << 16, w & 0xFFFF0000u); }
-
 // The 16-point transform Q = 1/4 H16 diag(s) on 16 pairs at once (two
 // independent vectors, one per half): the butterfly with strides 1, 2, 4, 8,
 // then * 0.25 + 0 in one rounding (as rht16_unsigned; the signs are applied
-// to the BF16 words before).
-__device__ __forceinline__ void rht16_pairs(uint64_t* p) {
+// to the BF16 words before).  Also returns each half's block amax
+// max_i |(Q x)_i|, exact.
+__device__ __forceinline__ void rht16_pairs(uint64_t* p, float& ma, float& mb) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       if ((i & h) == 0) {
@@ -301,39 +266,50 @@ __device__ __forceinline__ void rht16_pairs(uint64_t* p) {
       }
     }
   }
+  // last stage (stride 8); max(|fl(a + b)|, |fl(a - b)|) = fl(|a| + |b|)
+  // (rounding is monotonic), so the block amax of each half is a quarter of
+  // the largest fl(|a| + |b|) over the 8 butterflies
+  float ta[8], tb[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t a = p[i], b = p[i + 8];
+    ta[i] = __fadd_rn(fabsf(f2_lo(a)), fabsf(f2_lo(b)));
+    tb[i] = __fadd_rn(fabsf(f2_hi(a)), fabsf(f2_hi(b)));
+    p[i] = f2_add(a, b);
+    p[i + 8] = f2_sub(a, b);
+  }
+  ma = __fmul_rn(fmax3(fmax3(ta[0], ta[1], ta[2]), fmax3(ta[3], ta[4], ta[5]), fmaxf(ta[6], ta[7])), 0.25f);
+  mb = __fmul_rn(fmax3(fmax3(tb[0], tb[1], tb[2]), fmax3(tb[3], tb[4], tb[5]), fmaxf(tb[6], tb[7])), 0.25f);
   const uint64_t quarter = f2_pack(0x3E800000u, 0x3E800000u), zero = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) p[i] = f2_fma(p[i], quarter, zero);
 }
 
-// One 1x16 block held as 8 pairs (elements 2j, 2j+1 in pair j): amax, scale,
-// 16 codes (8 bytes).  Same arithmetic as quantize16.
+// One 1x16 block given as 8 BF16 words (elements 2j, 2j+1 in word j): amax
+// (a max over the BF16 magnitudes, exact), scale, 16 codes (8 bytes), the
+// values scaled as float pairs.  Same results as quantize16.
 template <bool kSR>
-__device__ __forceinline__ uint2 quantize16_pairs(const uint64_t* p, float s_enc, const float* enc_tab, uint32_t& E,
+__device__ __forceinline__ uint2 quantize16_words(const uint32_t* w, float s_enc, const float* enc_tab, uint32_t& E,
                                                   const PhiloxKey& key, uint32_t stream, uint64_t e0) {
-  float m = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(f2_lo(p[j])), fabsf(f2_hi(p[j]))));
+  const uint32_t m2 = bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(w[0], w[1]), bf16x2_absmax(w[2], w[3])),
+                                    bf16x2_absmax(bf16x2_absmax(w[4], w[5]), bf16x2_absmax(w[6], w[7])));
+  const float m = fmaxf(fabsf(bf16lo(m2)), fabsf(bf16hi(m2)));
   float enc;
   block_scale_tab(m, s_enc, enc_tab, E, enc);
   const uint64_t enc2 = f2_pack(__float_as_uint(enc), __float_as_uint(enc));
   float s[16];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const uint64_t q = f2_mul(p[j], enc2);
+    const uint64_t q = f2_mul(f2_from_bf16x2(w[j]), enc2);
     s[2 * j] = f2_lo(q);
     s[2 * j + 1] = f2_hi(q);
   }
   if constexpr (kSR) {
     uint32_t nu[16];
     sr_nu16(key, stream, e0, nu);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = e2m1_sr_value(s[i], nu[i]);
+    return sr_codes16(s, nu);
   }
-  uint2 out;
-  out.x = e2m1x8_rn(s);
-  out.y = e2m1x8_rn(s + 8);
-  return out;
+  return make_uint2(e2m1x8_rn(s), e2m1x8_rn(s + 8));
 }
 
 // ---------------------------------------------------------------------------
@@ -415,12 +391,10 @@ __global__ void __launch_bounds__(kThreads, 3) quant_tile_kernel(const uint16_t*
       for (int b = 0; b < 2; ++b) {
         const uint4* sp = reinterpret_cast<const uint4*>(&tile[r * kTilePitch + (hb + b) * 16]);
         const uint4 w0 = sp[0], w1 = sp[1];
-        const uint64_t pr[8] = {f2_from_bf16x2(w0.x), f2_from_bf16x2(w0.y), f2_from_bf16x2(w0.z),
-                                f2_from_bf16x2(w0.w), f2_from_bf16x2(w1.x), f2_from_bf16x2(w1.y),
-                                f2_from_bf16x2(w1.z), f2_from_bf16x2(w1.w)};
+        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         uint32_t E;
         const uint2 o =
-            quantize16_pairs<kSR>(pr, s_row, enc_tab[0], E, key, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
+            quantize16_words<kSR>(wv, s_row, enc_tab[0], E, key, orow.stream, (uint64_t)(gr * cols + gc + 16 * b));
         cw[2 * b] = o.x;
         cw[2 * b + 1] = o.y;
         sc |= E << (8 * b);
@@ -437,15 +411,18 @@ __global__ void __launch_bounds__(kThreads, 3) quant_tile_kernel(const uint16_t*
         if constexpr (kRHT) w ^= rht_sign_word(smask, i);  // both columns are in row i
         p[i] = f2_from_bf16x2(w);
       }
-      if constexpr (kRHT) rht16_pairs(p);
       const int64_t gm = m0 + 16 * ch;  // column of the transposed tensor
       // the block of each column: amax and scale, then both columns scaled
       // as pairs
       float ma = 0.0f, mb = 0.0f;
+      if constexpr (kRHT) {
+        rht16_pairs(p, ma, mb);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        ma = fmaxf(ma, fabsf(f2_lo(p[i])));
-        mb = fmaxf(mb, fabsf(f2_hi(p[i])));
+        for (int i = 0; i < 16; ++i) {
+          ma = fmaxf(ma, fabsf(f2_lo(p[i])));
+          mb = fmaxf(mb, fabsf(f2_hi(p[i])));
+        }
       }
       uint32_t Ea, Eb;
       float enca, encb;
@@ -463,13 +440,15 @@ __global__ void __launch_bounds__(kThreads, 3) quant_tile_kernel(const uint16_t*
       for (int h = 0; h < 2; ++h) {
         float* s = h ? sb : sa;
         const int64_t gr = c0 + pc + h;  // row of the transposed tensor
+        uint2 o;
         if constexpr (kSR) {
           uint32_t nu[16];
           sr_nu16(key, ot.stream, (uint64_t)(gr * rows + gm), nu);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) s[i] = e2m1_sr_value(s[i], nu[i]);
+          o = sr_codes16(s, nu);
+        } else {
+          o = make_uint2(e2m1x8_rn(s), e2m1x8_rn(s + 8));
         }
-        *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = make_uint2(e2m1x8_rn(s), e2m1x8_rn(s + 8));
+        *reinterpret_cast<uint2*>(ot.codes + gr * (rows >> 1) + (gm >> 1)) = o;
         ot.scales[sf_offset(ot.layout, gr, gm >> 4, rows >> 4)] = (uint8_t)(h ? Eb : Ea);
       }
     }

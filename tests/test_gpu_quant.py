@@ -136,6 +136,40 @@ def test_edge_values_and_ties():
         assert_q_equal(out, ref, what="edge " + name)
 
 
+def test_subnormal_only_blocks_of_a_tiny_tensor():
+    """Blocks that hold nothing but BF16 subnormals, in a tensor whose max is
+    so small that those blocks get a nonzero E4M3 scale: every block max (the
+    BF16-packed maxima of the rowwise blocks, the float maxima of the
+    transposed blocks, the sums taken for the transformed blocks) must see the
+    subnormals, not flush them.  Their enc overflows to inf, so their codes
+    saturate at +-6 on both sides."""
+    rng = np.random.default_rng(12)
+    rows, cols = 128, 256
+    x = (rng.standard_normal((rows, cols)) * 1e-34).astype(np.float32)
+    x[0, 0] = 1e-33
+    i = np.arange(16)
+    x[3, 16:32] = np.float32(2.0 ** -129) * (1 + i % 3)      # rowwise blocks
+    x[5, 32:48] = -np.float32(2.0 ** -130) * (1 + i % 5)
+    x[16:32, 64] = np.float32(2.0 ** -129) * (1 + i % 4)     # a transposed block
+    x[32:48, 100] = 0.0                                      # transformed: all 16 outputs +-2^-127
+    x[40, 100] = np.float32(2.0 ** -125)
+    xb = workloads.to_bf16(x)
+    xf = f32(xb)
+    assert np.all(np.abs(xf[3, 16:32]) < 2.0 ** -126) and np.all(xf[3, 16:32] != 0)
+    ref = quant.quantize_1d(xf, "rne")
+    for rht in (False, True):
+        ref_t = quant.quantize_transpose(xf, "rne", rht_seed=5 if rht else None)
+        out, out_t = B.nvfp4_quantize(xb.cuda(), B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, B.NVFP4_ROUND_RNE, rht=rht, seed=5)
+        assert_q_equal(out, ref, what="fused rowwise rht=%s" % rht)
+        assert_q_equal(out_t, ref_t, what="fused transpose rht=%s" % rht)
+        out_t, _ = B.nvfp4_quantize(xb.cuda(), B.NVFP4_Q_TRANSPOSE, B.NVFP4_ROUND_RNE, rht=rht, seed=5)
+        assert_q_equal(out_t, ref_t, what="transpose rht=%s" % rht)
+    out, _ = B.nvfp4_quantize(xb.cuda(), B.NVFP4_Q_ROWWISE, B.NVFP4_ROUND_RNE)
+    assert_q_equal(out, ref, what="rowwise")
+    for blk in ((3, 1), (5, 2)):
+        assert ref["scales"][blk] != 0
+
+
 def test_zero_tensor():
     """amax = 0: s_enc = ts = 1 and every scale is 0.  The rowwise codes are
     +0; the Hadamard sign flips give signed zeros in the transposed output,
