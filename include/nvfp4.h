@@ -414,8 +414,9 @@ void nvfp4_debug_stall_next_gemm(int32_t on);
 /*
  * nvfp4_debug_stall_next_quantize -- the same test hook for the quantize
  * kernels fed by a TMA tile pipeline (nvfp4_quantize_mx, and nvfp4_quantize
- * of the rowwise round-to-nearest-even kinds and of NVFP4_Q_2D).  With on != 0, the next such
- * launch never loads the first tile of its first CTA; that CTA's wait for it
+ * of every round-to-nearest-even kind and of NVFP4_Q_2D).  With on != 0, the
+ * next such launch never loads the first tile of its first CTA; that CTA's
+ * wait for it
  * runs into its bound (about 2 s), the kernel stops, waits (bounded) for the
  * loads it did issue and returns; nvfp4_get_status then reports
  * NVFP4_ERR_TIMEOUT and the CUDA context stays usable.  The output of that

@@ -323,6 +323,9 @@ __device__ __forceinline__ uint2 quantize16_words(const uint32_t* w, float s_enc
 // blocks; transposed, the column pair 2(t%32), 2(t%32)+1 over the 16 rows
 // 16(t/32)..16(t/32)+15 (one 32-bit shared-memory word per row), the two
 // columns carried as float pairs through the transform and the scaling.
+// Launched for the stochastic-rounding kinds, which are bound by instruction
+// issue (Philox draws and the rounding itself): 3 CTAs of 8 warps per SM keep
+// more warps to issue from than the ring kernel below, and measured faster.
 // ---------------------------------------------------------------------------
 struct TileOut {
   uint8_t* codes;
@@ -455,6 +458,143 @@ __global__ void __launch_bounds__(kThreads, 3) quant_tile_kernel(const uint16_t*
   }
 }
 
+// Barrier of the 256 consumer threads of the ring kernels (named barrier 1;
+// the producer warp does not take part).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// The same fused quantization with round-to-nearest-even on the TMA tile
+// ring (tile_ring.cuh), for the kinds that are bound by memory traffic: each
+// 128 x 64 tile is read once into the shared-memory ring; thread t has the
+// roles of quant_tile_kernel (rowwise, row t/2 and elements 32 (t%2) .. +31:
+// 8 threads of a quarter warp read 8 different swizzle chunks; transposed,
+// the column pair 2(t%32), 2(t%32)+1 over rows 16(t/32) .. +15: a warp reads
+// one whole 128-byte row).  The transposed codes and scales of a tile are
+// collected in shared memory (double-buffered) and stored as whole 64-byte
+// row segments and 4-byte scale words; the rowwise scales of a row go out as
+// one word.  The stochastic-rounding kinds, bound by instruction issue, keep
+// quant_tile_kernel, which runs 24 warps per SM against this kernel's 16.
+// ---------------------------------------------------------------------------
+constexpr int kTileRingCtas = 2;  // CTAs per SM (registers: up to 112 a thread)
+
+template <bool kRow, bool kT, bool kRHT>
+__global__ void __launch_bounds__(kRingThreads, kTileRingCtas)
+    quant_tile_ring_kernel(const __grid_constant__ CUtensorMap xmap, int64_t rows, int64_t cols, TileOut orow,
+                      TileOut ot, uint64_t seed, uint32_t* status,
+                      int debug_stall) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float enc_tab[2][128];
+  __shared__ __align__(16) uint2 tbuf[2][8 * 64];  // [buffer][token chunk * 64 + swizzled transposed row]
+  __shared__ __align__(4) uint8_t tE[2][64 * 8];   // [buffer][transposed row * 8 + token chunk]
+  int buf = 0;
+  const int t = threadIdx.x;
+  const PhiloxKey key{};  // round-to-nearest-even draws no random numbers
+  float s_row = 1.0f, s_t = 1.0f;
+  if constexpr (kRow) s_row = tensor_prologue(orow.amax, orow.ts, status);
+  if constexpr (kT) s_t = tensor_prologue(ot.amax, ot.ts, status);
+  if constexpr (kRow) fill_enc_table(enc_tab[0], s_row, t);
+  if constexpr (kT) fill_enc_table(enc_tab[1], s_t, t - 128);
+  // sign mask of the transform in both halves: row i's flip is bit 15 and
+  // bit 31 of (P << (15 - i)), the sign bits of the two BF16 values of a word
+  const uint32_t P = kRHT ? rht_sign_mask(seed) * 0x00010001u : 0u;
+  // rowwise role
+  const int r = t >> 1, hh = t & 1;
+  uint32_t roff[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) roff[i] = ring_chunk(r, 4 * hh + i);
+  // transposed role: rows 16 ch + i; the 16-byte chunk of the column pair
+  // sits at j ^ i (i % 8) in row 16 ch + i
+  const int pc = (t & 31) * 2, ch = t >> 5;
+  const uint32_t t_base = (uint32_t)(16 * ch * 128 + (pc & 7) * 2), j16 = (uint32_t)((pc >> 3) << 4);
+  tile_ring(&xmap, rows, cols, status, debug_stall, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
+    if (kRow && r < valid) {
+      const int64_t gr = m0 + r, gc = c0 + 32 * hh;
+      uint32_t cw[4], sc = 0;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint4 w0 = lds128(tile + roff[2 * b]), w1 = lds128(tile + roff[2 * b + 1]);
+        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        uint32_t E;
+        const uint2 o =
+            quantize16_words<false>(wv, s_row, enc_tab[0], E, key, 0, 0);
+        cw[2 * b] = o.x;
+        cw[2 * b + 1] = o.y;
+        sc |= E << (8 * b);
+      }
+      *reinterpret_cast<uint4*>(orow.codes + gr * (cols >> 1) + (gc >> 1)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      // the row's 4 scales of this tile (threads 2r, 2r + 1) as one word
+      const uint32_t sc4 = sc | (__shfl_down_sync(0xFFFFFFFFu, sc, 1) << 16);
+      if (hh == 0)
+        *reinterpret_cast<uint32_t*>(orow.scales + sf_offset(orow.layout, gr, c0 >> 4, cols >> 4)) = sc4;
+    }
+    if (kT) {
+      // the transposed codes and scales of this tile go through shared
+      // memory (double-buffered), so that the stores to global memory are
+      // whole 64-byte row segments and 4-byte scale words
+      uint2* tb = tbuf[buf];
+      uint8_t* te = tE[buf];
+      if (16 * ch < valid) {
+        uint64_t p[16];
+        uint32_t rowp[8];  // tile + row base + swizzled chunk for rows i and i + 8
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rowp[i] = (tile + t_base) + (j16 ^ (uint32_t)(i << 4));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          uint32_t w = lds32(rowp[i & 7] + (uint32_t)(i * 128));
+          if constexpr (kRHT) w ^= (P << (15 - i)) & 0x80008000u;  // both columns are in row i
+          p[i] = f2_from_bf16x2(w);
+        }
+        // the block of each column: amax and scale, then both columns scaled
+        // as pairs
+        float ma = 0.0f, mb = 0.0f;
+        if constexpr (kRHT) {
+          rht16_pairs(p, ma, mb);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            ma = fmaxf(ma, fabsf(f2_lo(p[i])));
+            mb = fmaxf(mb, fabsf(f2_hi(p[i])));
+          }
+        }
+        uint32_t Ea, Eb;
+        float enca, encb;
+        block_scale_tab(ma, s_t, enc_tab[1], Ea, enca);
+        block_scale_tab(mb, s_t, enc_tab[1], Eb, encb);
+        const uint64_t enc2 = f2_pack(__float_as_uint(enca), __float_as_uint(encb));
+        float sa[16], sb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t v = f2_mul(p[i], enc2);
+          sa[i] = f2_lo(v);
+          sb[i] = f2_hi(v);
+        }
+        const uint2 o[2] = {make_uint2(e2m1x8_rn(sa), e2m1x8_rn(sa + 8)), make_uint2(e2m1x8_rn(sb), e2m1x8_rn(sb + 8))};
+        // transposed rows pc, pc + 1 of token chunk ch: 16 bytes at row
+        // position pc ^ 2 ch of chunk ch's 64-row column
+        *reinterpret_cast<uint4*>(tb + ch * 64 + (pc ^ (2 * ch))) = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+        te[pc * 8 + ch] = (uint8_t)Ea;
+        te[(pc + 1) * 8 + ch] = (uint8_t)Eb;
+      }
+      consumer_sync();
+      {  // thread t: transposed row k = t / 4, token chunks 2q, 2q + 1
+        const int k = t >> 2, q = t & 3;
+        if (32 * q < valid) {
+          const uint2 a = tb[(2 * q) * 64 + (k ^ (4 * q))], b = tb[(2 * q + 1) * 64 + (k ^ (4 * q + 2))];
+          *reinterpret_cast<uint4*>(ot.codes + (c0 + k) * (rows >> 1) + (m0 >> 1) + 16 * q) =
+              make_uint4(a.x, a.y, b.x, b.y);
+        }
+      }
+      if (t < 128) {  // scale word g (4 token chunks) of transposed row k
+        const int k = t >> 1, g = t & 1;
+        if (64 * g < valid)
+          *reinterpret_cast<uint32_t*>(ot.scales + sf_offset(ot.layout, c0 + k, (m0 >> 4) + 4 * g, rows >> 4)) =
+              *reinterpret_cast<const uint32_t*>(te + k * 8 + 4 * g);
+      }
+      buf ^= 1;
+    }
+  });
+}
+
 // ---------------------------------------------------------------------------
 // 2D weight quantization on the TMA tile ring (tile_ring.cuh): 128 x 64 tiles
 // (8 x 4 blocks of 16 x 16) stream into a shared-memory ring while the 8
@@ -474,7 +614,6 @@ __global__ void __launch_bounds__(kThreads, 3) quant_tile_kernel(const uint16_t*
 // Two barriers of the 256 consumer threads per tile (named barrier 1; the
 // ring's producer warp does not take part).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kRingThreads, 3)
     quant_2d_ring_kernel(const __grid_constant__ CUtensorMap wmap, int64_t rows, int64_t cols, const float* amax,
@@ -674,24 +813,60 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
   if (out_row) orow = TileOut{out_row->codes, out_row->scales, amax_row, out_row->tensor_scale, out_row->scale_layout,
                               stream_row};
   if (out_t) ot = TileOut{out_t->codes, out_t->scales, amax_t, out_t->tensor_scale, out_t->scale_layout, stream_t};
+  const bool row = out_row != nullptr, tr = out_t != nullptr;
+  uint32_t* status = device_status_ptr();
+  if (!sr) {  // round-to-nearest-even: the ring kernel
+    const int64_t tiles = ring_tiles(rows, cols);
+    if (tiles >= kRingMaxTiles) return cudaErrorInvalidValue;
+    CUtensorMap map;
+    if (!make_ring_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto run = [&](auto kern, bool* attr_set) -> cudaError_t {
+      if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+      }
+      kern<<<ring_grid(tiles, kTileRingCtas), kRingThreads, kRingSmemBytes, s>>>(map, rows, cols, orow, ot, seed,
+                                                                                  status, take_ring_debug_stall());
+      count_launch();
+      return cudaGetLastError();
+    };
+#define NVFP4_RING(R, T, H)                                \
+  do {                                                     \
+    static bool attr_set[64] = {false};                    \
+    return run(quant_tile_ring_kernel<R, T, H>, attr_set); \
+  } while (0)
+    if (row && tr) {
+      if (rht_t) NVFP4_RING(true, true, true);
+      NVFP4_RING(true, true, false);
+    }
+    if (tr) {
+      if (rht_t) NVFP4_RING(false, true, true);
+      NVFP4_RING(false, true, false);
+    }
+    NVFP4_RING(true, false, false);
+#undef NVFP4_RING
+  }
+  // stochastic rounding: the register-staged tile kernel
   const int64_t tiles = ((rows + kTileRows - 1) / kTileRows) * (cols / kTile);
   if (tiles >= kMaxUnits) return cudaErrorInvalidValue;
   const int64_t cap = (int64_t)sm_count() * 8;
   const dim3 grid((unsigned)(tiles < cap ? (tiles > 0 ? tiles : 1) : cap));
-  uint32_t* status = device_status_ptr();
   const uint16_t* xp = static_cast<const uint16_t*>(x);
-  const bool row = out_row != nullptr, tr = out_t != nullptr;
   const PhiloxKey key = philox_key(seed);
-#define NVFP4_TILE(R, T, H, S) \
-  quant_tile_kernel<R, T, H, S><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot, seed, key, status)
+#define NVFP4_TILE(R, T, H) \
+  quant_tile_kernel<R, T, H, true><<<grid, kThreads, 0, s>>>(xp, rows, cols, orow, ot, seed, key, status)
   if (row && tr) {
-    if (rht_t) { if (sr) NVFP4_TILE(true, true, true, true); else NVFP4_TILE(true, true, true, false); }
-    else       { if (sr) NVFP4_TILE(true, true, false, true); else NVFP4_TILE(true, true, false, false); }
+    if (rht_t) NVFP4_TILE(true, true, true);
+    else NVFP4_TILE(true, true, false);
   } else if (tr) {
-    if (rht_t) { if (sr) NVFP4_TILE(false, true, true, true); else NVFP4_TILE(false, true, true, false); }
-    else       { if (sr) NVFP4_TILE(false, true, false, true); else NVFP4_TILE(false, true, false, false); }
+    if (rht_t) NVFP4_TILE(false, true, true);
+    else NVFP4_TILE(false, true, false);
   } else {
-    if (sr) NVFP4_TILE(true, false, false, true); else NVFP4_TILE(true, false, false, false);
+    NVFP4_TILE(true, false, false);
   }
 #undef NVFP4_TILE
   count_launch();

@@ -11,7 +11,7 @@ import torch
 from nvfp4_bit_numerics_gb300 import binding as B
 from nvfp4_bit_numerics_gb300 import workloads
 from oracle import formats, mx, quant
-from tests.gpu_util import ensure_lib, f32, outlier_tensor, rel_fro
+from tests.gpu_util import assert_q_equal, ensure_lib, f32, outlier_tensor, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -233,7 +233,7 @@ def test_mx_full_size_sampled():
     assert rel_fro(ys, formats.float64_to_bf16_rne(mx.gemm_mx_ref(rx, rw))) <= 1e-3
 
 
-@pytest.mark.parametrize("which", ["mxfp4", "nvfp4_rowwise_rne", "nvfp4_2d"])
+@pytest.mark.parametrize("which", ["mxfp4", "nvfp4_rowwise_rne", "nvfp4_2d", "nvfp4_fused_rne"])
 def test_tile_ring_wait_bound_reports_timeout(which):
     """Failure detection without a GPU fault for the TMA-ring quantizers: the
     test hook makes the next launch skip its first CTA's first tile load, the
@@ -251,6 +251,8 @@ def test_tile_ring_wait_bound_reports_timeout(which):
             return B.nvfp4_quantize_mx(xg, B.NVFP4_Q_ROWWISE)[0]
         if which == "nvfp4_2d":
             return B.nvfp4_quantize(xg, B.NVFP4_Q_2D)
+        if which == "nvfp4_fused_rne":
+            return B.nvfp4_quantize(xg, B.NVFP4_Q_ROWWISE_AND_TRANSPOSE, B.NVFP4_ROUND_RNE, rht=True, seed=4)
         return B.nvfp4_quantize(xg, B.NVFP4_Q_ROWWISE, B.NVFP4_ROUND_RNE)[0]
 
     assert B.nvfp4_get_status() == B.NVFP4_OK
@@ -265,13 +267,12 @@ def test_tile_ring_wait_bound_reports_timeout(which):
     assert B.nvfp4_get_status() == B.NVFP4_OK
     if which == "mxfp4":
         assert_mx_equal(q, mx.quantize_mx(xf), what="after the timeout")
+    elif which == "nvfp4_fused_rne":
+        assert_q_equal(q[0], quant.quantize_1d(xf, "rne"), what="rowwise after the timeout")
+        assert_q_equal(q[1], quant.quantize_transpose(xf, "rne", rht_seed=4), what="transposed after the timeout")
     elif which == "nvfp4_2d":
-        from tests.gpu_util import assert_q_equal
-
         r = quant.quantize_2d(xf)
         assert_q_equal(q[0], dict(codes=r["codes"], scales=r["scales"], amax=r["amax"], ts=r["ts"]), what="W")
         assert_q_equal(q[1], dict(codes=r["codes_t"], scales=r["scales_t"], amax=r["amax"], ts=r["ts"]), what="W^T")
     else:
-        from tests.gpu_util import assert_q_equal
-
         assert_q_equal(q, quant.quantize_1d(xf, "rne"), what="after the timeout")
