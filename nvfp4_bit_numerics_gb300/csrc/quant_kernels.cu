@@ -600,8 +600,9 @@ __global__ void __launch_bounds__(kRingThreads, kTileRingCtas)
 // (8 x 4 blocks of 16 x 16) stream into a shared-memory ring while the 8
 // consumer warps encode them.
 //  - block pass: the 8 threads (consecutive lanes) of block (br, bc) hold
-//    rows p and p + 8 of it; the block amax is a shuffle over the 8; each
-//    thread encodes its two rows (W codes, K-major, 8 bytes per row).
+//    rows p and p + 8 of it; the block amax is a max over BF16 pairs, then a
+//    shuffle over the 8; each thread encodes its two rows (W codes, K-major,
+//    8 bytes per row).
 //  - scales: one 32-bit word per row of W (its 4 blocks of the tile) and two
 //    per row of W^T (its 8 blocks), from the tile's 32 block scales.
 //  - column pass: thread (cp, brr) encodes the 16 x 2 slice (columns 2 cp,
@@ -609,19 +610,22 @@ __global__ void __launch_bounds__(kRingThreads, kTileRingCtas)
 //    word per row (a warp reads one whole 128-byte row: no bank conflicts);
 //    encoding an element twice gives the same code, so W^T is exactly W
 //    transposed.  The W^T codes of the tile (64 rows of 64 bytes) are
-//    collected in shared memory and written as one 16-byte store per thread,
-//    whole sectors per row.
-// Two barriers of the 256 consumer threads per tile (named barrier 1; the
-// ring's producer warp does not take part).
+//    collected in shared memory, swizzled so that neither the 16-byte writes
+//    nor the 8-byte reads conflict, and written after the next tile's
+//    barrier as one 16-byte store per thread, whole sectors per row.
+// Block scales and W^T codes are double-buffered, so one barrier of the 256
+// consumer threads per tile orders everything.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kRingThreads, 3)
     quant_2d_ring_kernel(const __grid_constant__ CUtensorMap wmap, int64_t rows, int64_t cols, const float* amax,
                          TileOut ow, TileOut owt, int has_t, uint32_t* status, int debug_stall) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float s_enc[8][4];
-  __shared__ uint32_t s_E[8][4];
-  __shared__ __align__(16) uint2 tbuf[64][8];  // W^T codes: [W^T row of the tile][block row]
+  // double-buffered per-tile state: block scales and the W^T codes, stored
+  // after the next tile's barrier (one barrier per tile)
+  __shared__ float s_enc[2][8][4];
+  __shared__ uint32_t s_E[2][8][4];
+  __shared__ __align__(16) uint2 tbuf[2][8 * 64];  // [buffer][block row * 64 + swizzled W^T row]
   const int t = threadIdx.x;
   const float s_tensor = tensor_prologue(amax, ow.ts, status);
   if (has_t && blockIdx.x == 0 && t == 0) *owt.ts = tensor_decode_scale(s_tensor);
@@ -633,20 +637,40 @@ __global__ void __launch_bounds__(kRingThreads, 3)
     roff[2 * h] = ring_chunk(16 * br + p + 8 * h, 2 * bc);
     roff[2 * h + 1] = ring_chunk(16 * br + p + 8 * h, 2 * bc + 1);
   }
-  // column pass role: column pair cp, block row brr; row i of the block at
-  // coff + 128 i (16 rows of one block share (i % 8) only through the
-  // swizzle, so the offset of each row is recomputed from a base)
+  // column pass role: column pair (2 cp, 2 cp + 1), block row brr; its 16-byte
+  // chunk of row 16 brr + i sits at (cp / 4) ^ (i % 8)
   const int cp = t & 31, brr = t >> 5;
+  const uint32_t t_base = (uint32_t)(16 * brr * 128 + (cp & 3) * 4), j16 = (uint32_t)((cp >> 2) << 4);
   const int64_t n_kb_w = cols >> 4, n_kb_t = rows >> 4;
+  int buf = 0;
+  bool pending = false;  // tbuf[buf ^ 1] holds the previous tile's W^T codes
+  int64_t pm0 = 0, pc0 = 0;
+  int pvalid = 0;
+  // thread t: W^T row t / 4 of tile (m0, c0), 16 bytes (block rows 2q, 2q + 1)
+  auto write_t = [&](int b, int64_t m0, int64_t c0, int valid) {
+    const int k = t >> 2, q = t & 3;
+    if (32 * q < valid) {
+      const uint2 lo = tbuf[b][(2 * q) * 64 + (k ^ (4 * q))], hi = tbuf[b][(2 * q + 1) * 64 + (k ^ (4 * q + 2))];
+      *reinterpret_cast<uint4*>(owt.codes + (c0 + k) * (rows >> 1) + (m0 >> 1) + 16 * q) =
+          make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+  };
   tile_ring(&wmap, rows, cols, status, debug_stall, smem_raw, [&](uint32_t tile, int64_t m0, int64_t c0, int valid) {
     // ---- block pass: amax, scale, W codes
     const bool row_ok = 16 * br < valid;
-    float v[32];
+    uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) unpack8(lds128(tile + roff[j]), v + 8 * j);
-    float m = 0.0f;
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = lds128(tile + roff[j]);
+      w[4 * j] = q.x;
+      w[4 * j + 1] = q.y;
+      w[4 * j + 2] = q.z;
+      w[4 * j + 3] = q.w;
+    }
+    uint32_t m2 = bf16x2_absmax(w[0], w[1]);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    for (int j = 2; j < 16; ++j) m2 = bf16x2_absmax(m2, w[j]);
+    float m = fmaxf(fabsf(bf16lo(m2)), fabsf(bf16hi(m2)));
     m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
     m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
@@ -654,67 +678,72 @@ __global__ void __launch_bounds__(kRingThreads, 3)
     float enc;
     block_scale(m, s_tensor, E, enc);
     if (p == 0) {
-      s_E[br][bc] = E;
-      s_enc[br][bc] = enc;
+      s_E[buf][br][bc] = E;
+      s_enc[buf][br][bc] = enc;
     }
     if (row_ok) {
+      const uint64_t enc2 = f2_pack(__float_as_uint(enc), __float_as_uint(enc));
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float sv[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sv[i] = __fmul_rn(v[16 * h + i], enc);
+        for (int j = 0; j < 8; ++j) {
+          const uint64_t v = f2_mul(f2_from_bf16x2(w[8 * h + j]), enc2);
+          sv[2 * j] = f2_lo(v);
+          sv[2 * j + 1] = f2_hi(v);
+        }
         const int64_t gr = m0 + 16 * br + p + 8 * h, gc = c0 + 16 * bc;
         *reinterpret_cast<uint2*>(ow.codes + gr * (cols >> 1) + (gc >> 1)) =
             make_uint2(e2m1x8_rn(sv), e2m1x8_rn(sv + 8));
       }
     }
     consumer_sync();
+    if (has_t && pending) write_t(buf ^ 1, pm0, pc0, pvalid);
     // ---- scales: W rows (4 blocks of the tile per word), W^T rows (4 block
     // rows per word)
     if (t < 128) {
       if (t < valid) {
         const int b = t >> 4;
-        const uint32_t w4 = s_E[b][0] | (s_E[b][1] << 8) | (s_E[b][2] << 16) | (s_E[b][3] << 24);
+        const uint32_t w4 =
+            s_E[buf][b][0] | (s_E[buf][b][1] << 8) | (s_E[buf][b][2] << 16) | (s_E[buf][b][3] << 24);
         *reinterpret_cast<uint32_t*>(ow.scales + sf_offset(ow.layout, m0 + t, c0 >> 4, n_kb_w)) = w4;
       }
     } else if (has_t) {
       const int u = t - 128, k = u >> 1, g = u & 1;
       if (64 * g < valid) {
         const int b = k >> 4;
-        const uint32_t w4 = s_E[4 * g][b] | (s_E[4 * g + 1][b] << 8) | (s_E[4 * g + 2][b] << 16) |
-                            (s_E[4 * g + 3][b] << 24);
+        const uint32_t w4 = s_E[buf][4 * g][b] | (s_E[buf][4 * g + 1][b] << 8) | (s_E[buf][4 * g + 2][b] << 16) |
+                            (s_E[buf][4 * g + 3][b] << 24);
         *reinterpret_cast<uint32_t*>(owt.scales + sf_offset(owt.layout, c0 + k, (m0 >> 4) + 4 * g, n_kb_t)) = w4;
       }
     }
-    if (!has_t) {
-      consumer_sync();  // s_E / s_enc are rewritten by the next tile
-      return;
-    }
-    // ---- column pass: W^T codes of this block row
-    if (16 * brr < valid) {
-      const float e = s_enc[brr][cp >> 3];
-      float va[16], vb[16];
+    if (has_t) {
+      // ---- column pass: W^T codes of this block row (encoding an element
+      // twice gives the same code, so W^T is exactly W transposed)
+      if (16 * brr < valid) {
+        const float e = s_enc[buf][brr][cp >> 3];
+        const uint64_t e2 = f2_pack(__float_as_uint(e), __float_as_uint(e));
+        uint32_t rowp[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = 16 * brr + i;
-        const uint32_t wd = lds32(tile + ring_chunk(r, cp >> 2) + ((cp & 3) << 2));
-        va[i] = __fmul_rn(bf16lo(wd), e);
-        vb[i] = __fmul_rn(bf16hi(wd), e);
+        for (int i = 0; i < 8; ++i) rowp[i] = (tile + t_base) + (j16 ^ (uint32_t)(i << 4));
+        float va[16], vb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t v = f2_mul(f2_from_bf16x2(lds32(rowp[i & 7] + (uint32_t)(i * 128))), e2);
+          va[i] = f2_lo(v);
+          vb[i] = f2_hi(v);
+        }
+        *reinterpret_cast<uint4*>(&tbuf[buf][brr * 64 + ((2 * cp) ^ (2 * brr))]) =
+            make_uint4(e2m1x8_rn(va), e2m1x8_rn(va + 8), e2m1x8_rn(vb), e2m1x8_rn(vb + 8));
       }
-      tbuf[2 * cp][brr] = make_uint2(e2m1x8_rn(va), e2m1x8_rn(va + 8));
-      tbuf[2 * cp + 1][brr] = make_uint2(e2m1x8_rn(vb), e2m1x8_rn(vb + 8));
+      pending = true;
+      pm0 = m0;
+      pc0 = c0;
+      pvalid = valid;
     }
-    consumer_sync();
-    // thread t: W^T row t / 4 of the tile, 16 bytes (block rows 2q, 2q + 1)
-    {
-      const int k = t >> 2, q = t & 3;
-      if (32 * q < valid) {
-        const uint2 a = tbuf[k][2 * q], b = tbuf[k][2 * q + 1];
-        *reinterpret_cast<uint4*>(owt.codes + (c0 + k) * (rows >> 1) + (m0 >> 1) + 16 * q) =
-            make_uint4(a.x, a.y, b.x, b.y);
-      }
-    }
+    buf ^= 1;
   });
+  if (has_t && pending) write_t(buf ^ 1, pm0, pc0, pvalid);  // after the ring's closing barrier
 }
 
 }  // namespace
