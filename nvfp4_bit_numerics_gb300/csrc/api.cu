@@ -468,9 +468,9 @@ nvfp4_status nvfp4_linear_bwd(const void* dy, int64_t M, int64_t K, int64_t N, u
     e = launch_quant_tile(dy, M, N, &v.dyq, v.dyq.amax, &v.dytq, v.dytq.amax, true, true, seed, kStreamDy,
                           kStreamDyT, s);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-  st = launch_gemm(v.dyq, v.wtq, dx, NVFP4_OUT_BF16, K, s);
-  if (st != NVFP4_OK) return st;
-  return launch_gemm(v.dytq, v.xtq, dw, NVFP4_OUT_BF16, K, s);
+  // Dgrad and Wgrad are independent: one launch for both when the CTA-pair
+  // kernel takes both
+  return launch_gemm2(v.dyq, v.wtq, dx, K, v.dytq, v.xtq, dw, K, s);
 }
 
 }  // extern "C"

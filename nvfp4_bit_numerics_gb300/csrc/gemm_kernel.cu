@@ -21,8 +21,11 @@
 // Two kernels.  For M and N multiples of 256, nvfp4_gemm_pair_kernel (CTA
 // pairs, 256 x 256 tiles, tcgen05.mma.cta_group::2, scale tiles loaded with
 // each operand stage and copied into tensor memory by tcgen05.cp from the
-// MMA warp; described before it below).  Otherwise the single-CTA kernel,
-// whose design is:
+// MMA warp; described before it below).  It runs one GEMM, or two
+// independent ones of the same operand format over one tile schedule (the
+// Dgrad and Wgrad of a layer: the second GEMM's tiles fill the rounds the
+// first leaves part-empty).  Otherwise the single-CTA kernel, whose design
+// is:
 // (one CTA per SM, persistent over 128 x BN output tiles)
 //   warp 0      TMA producer: 2D tiled loads of the packed codes (128-byte
 //               rows, 128B swizzle) and 1D bulk loads of the scale tiles,
@@ -514,6 +517,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 //               values (amax_out) and quantizes its row's 128 BF16 values to
 //               NVFP4 1x16 blocks with a given tensor amax (q_codes), writing
 //               the codes and MMA-layout scales itself.
+// Persistent: pair q of P walks its tiles in order, all three roles
+// computing the same sequence.  One GEMM: tiles q, q + P, ...  Two GEMMs
+// (kTwo; the second one's maps and parameters in g1): the PairSched order
+// below, in which the pairs that the first GEMM's last round leaves idle start
+// on the second one early.  The per-tile work is the same in both modes, so a
+// GEMM gives the same bits either way.
 // ---------------------------------------------------------------------------
 constexpr int kPairBN = 256;
 constexpr int kPairABytes = 128 * kBKBytes;  // per CTA
@@ -533,6 +542,72 @@ constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kPairEpiWarps * k
 static_assert(kPairSmemBytes <= 232448, "pair kernel shared memory exceeds the 227 KB opt-in limit");
 constexpr int kPairThreads = 32 * (kPairFirstEpiWarp + kPairEpiWarps);
 constexpr uint64_t kDrainNs = 50000;  // after an abort: time for loads already issued to land
+
+// One GEMM of a pair-kernel launch: its operand, scale and output maps and
+// its parameters.  A launch runs one GEMM, or two of the same operand format
+// (the Dgrad and Wgrad of a layer) over one tile schedule.
+struct alignas(64) PairProblem {
+  CUtensorMap a, b, sfa, sfb, d;
+  Params p;
+};
+
+// Tile schedule of a launch over P CTA pairs: the n0 tiles of problem 0 go
+// round-robin (pair q takes q, q + P, ...; the first rem0 = n0 % P pairs take
+// one more, "long" pairs), then the n1 tiles of problem 1: k1 head rounds over
+// the S = P - rem0 short pairs only (they start on problem 1 one problem-0 tile
+// earlier), then round-robin over all pairs.  Every tile of each problem goes
+// to exactly one pair; consecutive tiles still run at the same time on
+// neighbouring pairs (the L2 reuse the tile order is chosen for).
+struct PairSched {
+  int n0, n1, P, rem0, k1;
+};
+
+// The i-th tile of `pair` (false once the pair has no more tiles).
+__device__ __forceinline__ bool pair_tile(const PairSched& sc, int pair, int i, int& prob, int& tile) {
+  const int c0 = (sc.n0 - pair + sc.P - 1) / sc.P;  // this pair's problem-0 tiles
+  if (i < c0) {
+    prob = 0;
+    tile = pair + i * sc.P;
+    return true;
+  }
+  const int i1 = i - c0, S = sc.P - sc.rem0;
+  int j;
+  if (pair >= sc.rem0 && i1 < sc.k1)
+    j = i1 * S + (pair - sc.rem0);
+  else
+    j = S * sc.k1 + (pair >= sc.rem0 ? i1 - sc.k1 : i1) * sc.P + pair;
+  if (j >= sc.n1) return false;
+  prob = 1;
+  tile = j;
+  return true;
+}
+
+// The tile sequence of a pair: pair_tile for two problems; for one, plain
+// round-robin over n_tiles with the tile index as the only loop variable.
+template <bool kTwo>
+struct TileIter {
+  const PairSched& sc;
+  int pair, it = 0, prob = 0, tile = 0;
+  bool ok;
+  __device__ __forceinline__ TileIter(const PairSched& s, int pr, int, int) : sc(s), pair(pr) {
+    ok = pair_tile(sc, pair, 0, prob, tile);
+  }
+  __device__ __forceinline__ void next() { ok = pair_tile(sc, pair, ++it, prob, tile); }
+};
+template <>
+struct TileIter<false> {
+  int prob = 0, tile, n, step;
+  bool ok;
+  __device__ __forceinline__ TileIter(const PairSched&, int pr, int n_tiles, int num_pairs)
+      : tile(pr), n(n_tiles), step(num_pairs) {
+    ok = tile < n;
+  }
+  __device__ __forceinline__ void next() {
+    tile += step;
+    ok = tile < n;
+  }
+};
+
 
 __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -633,10 +708,12 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+template <bool kTwo>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
-                           const __grid_constant__ CUtensorMap tmap_d, Params p) {
+                           const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ Params p,
+                           const __grid_constant__ PairProblem g1, const PairSched sched) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -676,6 +753,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_sfa)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_sfb)) : "memory");
+    if constexpr (kTwo) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g1.a)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g1.b)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g1.sfa)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g1.sfb)) : "memory");
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -694,13 +777,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = pair; tile < n_tiles; tile += num_pairs) {
-        int mb, nb;
-        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
+      for (TileIter<kTwo> ti(sched, pair, n_tiles, num_pairs); ti.ok; ti.next()) {
+        const int tile = ti.tile;
+        // the tile's problem: problem 0 in the kernel's own parameters, 1 in g1
+        const bool second = kTwo && ti.prob;
+        const CUtensorMap* map_a = second ? &g1.a : &tmap_a;
+        const CUtensorMap* map_b = second ? &g1.b : &tmap_b;
+        const CUtensorMap* map_sfa = second ? &g1.sfa : &tmap_sfa;
+        const CUtensorMap* map_sfb = second ? &g1.sfb : &tmap_sfb;
+        int mb, nb, t_stages = k_stages;
+        if constexpr (kTwo) {
+          const Params& gp = second ? g1.p : p;
+          tile_coords(tile, gp.M / 256, gp.N / kPairBN, gp.n_fastest, mb, nb);
+          t_stages = (gp.K + kKPerStage - 1) / kKPerStage;
+        } else {
+          tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
+        }
         bool ok = true;
-        for (int ks = 0; ks < k_stages; ++ks) {
+        for (int ks = 0; ks < t_stages; ++ks) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort, p.status)) { ok = false; break; }
-          if (p.debug_stall && tile == pair && ks == 0) {
+          if (p.debug_stall && tile == pair && !second && ks == 0) {
             // nothing is issued or armed for this stage: the MMA warp's
             // bounded wait runs out and the kernel reports NVFP4_ERR_TIMEOUT
             if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
@@ -709,12 +805,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           const uint32_t sa = base + stage * kPairStageBytes;
           const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * kPairStageBytes);
-          tma_load_2d_pair(sa, &tmap_a, ks * kBKBytes, mb * 256 + (int)rank * 128, leader_full);
-          tma_load_2d_pair(sa + kPairABytes, &tmap_b, ks * kBKBytes, nb * kPairBN + (int)rank * 128, leader_full);
+          tma_load_2d_pair(sa, map_a, ks * kBKBytes, mb * 256 + (int)rank * 128, leader_full);
+          tma_load_2d_pair(sa + kPairABytes, map_b, ks * kBKBytes, nb * kPairBN + (int)rank * 128, leader_full);
           // scale tiles as 8-byte words: 4 tiles (2 KB) of this CTA's A rows,
           // 4 tiles of each of the two 128-row halves of B
-          tma_load_2d_pair(sa + kPairABytes + kPairBBytes, &tmap_sfa, ks * 256, 2 * mb + (int)rank, leader_full);
-          tma_load_2d_pair(sa + kPairABytes + kPairBBytes + kPairSfaBytes, &tmap_sfb, ks * 256, 2 * nb,
+          tma_load_2d_pair(sa + kPairABytes + kPairBBytes, map_sfa, ks * 256, 2 * mb + (int)rank, leader_full);
+          tma_load_2d_pair(sa + kPairABytes + kPairBBytes + kPairSfaBytes, map_sfb, ks * 256, 2 * nb,
                            leader_full);
           if (++stage == kPairStages) { stage = 0; phase ^= 1u; }
         }
@@ -758,10 +854,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = pair; tile < n_tiles && ok; tile += num_pairs) {
+      for (TileIter<kTwo> ti(sched, pair, n_tiles, num_pairs); ok && ti.ok; ti.next()) {
+        int k_stages_t = k_stages, last_nk_t = last_nk;
+        if constexpr (kTwo) {
+          const Params& gp = ti.prob ? g1.p : p;
+          k_stages_t = (gp.K + kKPerStage - 1) / kKPerStage;
+          last_nk_t = ((gp.K - 1) % kKPerStage) / kMmaK + 1;
+        }
         if (!warp_wait(tmem_empty, acc_phase ^ 1u)) break;
         tc_fence_after();
-        for (int ks = 0; ks < k_stages; ++ks) {
+        for (int ks = 0; ks < k_stages_t; ++ks) {
           if (!stage_wait(full_bar(stage), phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t soff = (uint64_t)stage * kStageDesc;
@@ -775,14 +877,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int j = 0; j < 4; ++j) tc_cp_sf_pair(sfb + 8 * j + 4 * h, dsf + (4 + 4 * h + j) * kTileDesc);
-            if (ks != k_stages - 1 || last_nk == 4) {
+            if (ks != k_stages_t - 1 || last_nk_t == 4) {
               tc_mma_pair(tmem_u, da, db, idesc, sfa, sfb, ks != 0, kMX);
               tc_mma_pair(tmem_u, da + 2, db + 2, idesc, sfa + 4, sfb + 8, 1u, kMX);
               tc_mma_pair(tmem_u, da + 4, db + 4, idesc, sfa + 8, sfb + 16, 1u, kMX);
               tc_mma_pair(tmem_u, da + 6, db + 6, idesc, sfa + 12, sfb + 24, 1u, kMX);
             } else {
               // +32 bytes along K per MMA inside the 128-byte swizzle atom
-              for (int j = 0; j < last_nk; ++j)
+              for (int j = 0; j < last_nk_t; ++j)
                 tc_mma_pair(tmem_u, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + 8 * j, (ks | j) != 0, kMX);
             }
             tc_commit_pair_multicast(empty_bar(stage));
@@ -822,10 +924,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         if (!(abs_bits(a) < 0x7F800000u)) raise_status(p.status, kStatusNonFinite);
       }
     }
+    if constexpr (kTwo) {  // the second problem's quantized output: its tensor scale
+      if (g1.p.q_codes && blockIdx.x == 0 && warp == kPairFirstEpiWarp && lane == 0) {
+        const float a = *g1.p.q_amax;
+        *g1.p.q_ts = tensor_decode_scale(tensor_encode_scale(a));
+        if (!(abs_bits(a) < 0x7F800000u)) raise_status(p.status, kStatusNonFinite);
+      }
+    }
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < n_tiles; tile += num_pairs) {
+    for (TileIter<kTwo> ti(sched, pair, n_tiles, num_pairs); ti.ok; ti.next()) {
+      const int tile = ti.tile;
+      // the tile's problem (with two problems, its scales and output are read
+      // per tile)
+      const bool second = kTwo && ti.prob;
+      const Params& tpp = second ? g1.p : p;
+      const CUtensorMap* map_d = second ? &g1.d : &tmap_d;
+      float alpha_t = alpha, q_senc_t = q_senc;
+      if (second) {
+        alpha_t = g1.p.mx ? 1.0f : __fmul_rn(*g1.p.ts_a, *g1.p.ts_b);
+        q_senc_t = g1.p.q_codes ? tensor_encode_scale(*g1.p.q_amax) : 1.0f;
+      }
       int mb, nb;
-        tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
+      if constexpr (kTwo) tile_coords(tile, tpp.M / 256, tpp.N / kPairBN, tpp.n_fastest, mb, nb);
+      else tile_coords(tile, num_m, num_n, p.n_fastest, mb, nb);
       int ready = 0;
       if (lane == 0) ready = mbar_wait(tmem_full, acc_phase, abort, p.status) ? 1 : 0;
       ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
@@ -845,19 +966,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_leader(tmem_empty, rank);
       acc_phase ^= 1u;
-      if (p.d_f32) {
+      if (tpp.d_f32) {
         uint32_t m32 = 0;  // max magnitude bits
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.d) + row * p.ldd + col0);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(tpp.d) + row * tpp.ldd + col0);
 #pragma unroll
         for (int i = 0; i < kCols / 4; ++i) {
-          const uint4 o = make_uint4(__float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i]))),
-                                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 1]))),
-                                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 2]))),
-                                     __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[4 * i + 3]))));
+          const uint4 o = make_uint4(__float_as_uint(__fmul_rn(alpha_t, __uint_as_float(v[4 * i]))),
+                                     __float_as_uint(__fmul_rn(alpha_t, __uint_as_float(v[4 * i + 1]))),
+                                     __float_as_uint(__fmul_rn(alpha_t, __uint_as_float(v[4 * i + 2]))),
+                                     __float_as_uint(__fmul_rn(alpha_t, __uint_as_float(v[4 * i + 3]))));
           dst[i] = o;
           m32 = max(m32, max(max(o.x & 0x7FFFFFFFu, o.y & 0x7FFFFFFFu), max(o.z & 0x7FFFFFFFu, o.w & 0x7FFFFFFFu)));
         }
-        if (p.amax_out) amax_bits_to_global(m32, p.amax_out);
+        if (tpp.amax_out) amax_bits_to_global(m32, tpp.amax_out);
       } else {
         // 16-column chunks, each one 1x16 block of the row: scaled and
         // rounded to BF16, then (as asked) folded into the output amax,
@@ -870,19 +991,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         uint32_t m2 = 0;               // max BF16 magnitude bits of both halves
         uint32_t sc[2] = {0u, 0u};     // quantized output: 8 block scales
         uint32_t qw[4] = {0u, 0u, 0u, 0u};
-        uint4* cdst = p.q_codes ? reinterpret_cast<uint4*>(p.q_codes + row * (p.N >> 1) + (col0 >> 1)) : nullptr;
+        uint4* cdst = tpp.q_codes ? reinterpret_cast<uint4*>(tpp.q_codes + row * (tpp.N >> 1) + (col0 >> 1)) : nullptr;
 #pragma unroll
         for (int j = 0; j < kCols / 16; ++j) {
           uint32_t pk[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            pk[i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(v[16 * j + 2 * i])),
-                                __fmul_rn(alpha, __uint_as_float(v[16 * j + 2 * i + 1])));
-          if (p.amax_out) {
+            pk[i] = pack_bf16x2(__fmul_rn(alpha_t, __uint_as_float(v[16 * j + 2 * i])),
+                                __fmul_rn(alpha_t, __uint_as_float(v[16 * j + 2 * i + 1])));
+          if (tpp.amax_out) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, pk[i] & 0x7FFF7FFFu);
           }
-          if (p.q_codes) {
+          if (tpp.q_codes) {
             // as the rowwise RNE quantizer would quantize the stored BF16 output
             float f[16];
 #pragma unroll
@@ -891,13 +1012,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
               f[2 * i + 1] = bf16hi(pk[i]);
             }
             uint32_t E;
-            const uint2 o = quantize16_rne(f, q_senc, E);
+            const uint2 o = quantize16_rne(f, q_senc_t, E);
             sc[j >> 2] |= E << (8 * (j & 3));
             qw[2 * (j & 1)] = o.x;
             qw[2 * (j & 1) + 1] = o.y;
             if (j & 1) cdst[j >> 1] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
           }
-          if (p.tma_store) {
+          if (tpp.tma_store) {
             if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
 #pragma unroll
@@ -909,14 +1030,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) tma_store_2d(&tmap_d, (int)col0 + 16 * j, (int)(row - lane), buf);
+            if (lane == 0) tma_store_2d(map_d, (int)col0 + 16 * j, (int)(row - lane), buf);
           }
         }
-        if (p.amax_out) amax_bits_to_global(max(m2 & 0xFFFFu, m2 >> 16) << 16, p.amax_out);
-        if (p.q_codes) {
-          const int64_t n_kb = p.N >> 4, kb0 = col0 >> 4;
-          *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0, n_kb)) = sc[0];
-          *reinterpret_cast<uint32_t*>(p.q_scales + sf_mma_offset(row, kb0 + 4, n_kb)) = sc[1];
+        if (tpp.amax_out) amax_bits_to_global(max(m2 & 0xFFFFu, m2 >> 16) << 16, tpp.amax_out);
+        if (tpp.q_codes) {
+          const int64_t n_kb = tpp.N >> 4, kb0 = col0 >> 4;
+          *reinterpret_cast<uint32_t*>(tpp.q_scales + sf_mma_offset(row, kb0, n_kb)) = sc[0];
+          *reinterpret_cast<uint32_t*>(tpp.q_scales + sf_mma_offset(row, kb0 + 4, n_kb)) = sc[1];
         }
       }
     }
@@ -1033,25 +1154,17 @@ nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t 
 }
 
 
-nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
-                      float* amax_out, const nvfp4_tensor* yq, cudaStream_t s) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) !=
-        cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    attr_set[dev] = true;
-  }
-  CUtensorMap ma, mb, msfa, msfb;
+// The maps and parameters of one GEMM of the pair kernel.
+nvfp4_status make_pair_problem(PairProblem& g, const nvfp4_tensor& a, const nvfp4_tensor& b, void* d,
+                               int32_t d_dtype, int64_t ldd, float* amax_out, const nvfp4_tensor* yq,
+                               int debug_stall) {
   const int64_t K = a.cols;
-  if (!make_code_map(&ma, a.codes, (uint64_t)K / 2, (uint64_t)a.rows, 128) ||
-      !make_code_map(&mb, b.codes, (uint64_t)K / 2, (uint64_t)b.rows, 128) ||
-      !make_sf_map(&msfa, a.scales, (uint64_t)K / 64, (uint64_t)a.rows / 128, 1) ||
-      !make_sf_map(&msfb, b.scales, (uint64_t)K / 64, (uint64_t)b.rows / 128, 2))
+  if (!make_code_map(&g.a, a.codes, (uint64_t)K / 2, (uint64_t)a.rows, 128) ||
+      !make_code_map(&g.b, b.codes, (uint64_t)K / 2, (uint64_t)b.rows, 128) ||
+      !make_sf_map(&g.sfa, a.scales, (uint64_t)K / 64, (uint64_t)a.rows / 128, 1) ||
+      !make_sf_map(&g.sfb, b.scales, (uint64_t)K / 64, (uint64_t)b.rows / 128, 2))
     return NVFP4_ERR_CUDA;
-  Params p;
+  Params& p = g.p;
   p.sfa = a.scales;
   p.sfb = b.scales;
   p.ts_a = a.tensor_scale;
@@ -1064,7 +1177,7 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   p.K = (int)K;
   p.sf_tiles_k = (int)(K / 64);
   p.n_fastest = p.N < p.M;
-  p.debug_stall = g_debug_stall.exchange(0);
+  p.debug_stall = debug_stall;
   p.status = device_status_ptr();
   p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
   p.mx = a.format == NVFP4_FORMAT_MXFP4;
@@ -1075,20 +1188,108 @@ nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int
   // BF16 output goes through bulk tensor stores (the API guarantees the
   // 16-byte aligned base and row stride they need); FP32 through plain
   // stores; no BF16 output (quantized output only) stores nothing
-  CUtensorMap md = ma;  // unused for FP32 or no BF16 output
+  g.d = g.a;  // unused for FP32 or no BF16 output
   p.tma_store = !p.d_f32 && d != nullptr;
-  if (p.tma_store && !make_out_map(&md, d, (uint64_t)p.N, (uint64_t)p.M, (uint64_t)ldd)) return NVFP4_ERR_CUDA;
-  const int tiles = (p.M / 256) * (p.N / kPairBN);
-  const int pairs_max = sm_count() / 2;
-  const int pairs = tiles < pairs_max ? tiles : pairs_max;
-  nvfp4_gemm_pair_kernel<<<2 * pairs, kPairThreads, kPairSmemBytes, s>>>(ma, mb, msfa, msfb, md, p);
+  if (p.tma_store && !make_out_map(&g.d, d, (uint64_t)p.N, (uint64_t)p.M, (uint64_t)ldd)) return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
+
+// The schedule of n0 tiles of k-length c0 and n1 tiles of k-length c1 over
+// P pairs (pair_tile): the number of head rounds k1 that gives the shortest
+// longest pair, found by counting every pair's stages.
+PairSched make_sched(int n0, int c0, int n1, int c1, int P) {
+  PairSched best{n0, n1, P, n1 ? n0 % P : 0, 0};
+  if (!n1 || best.rem0 == 0) return best;
+  int64_t best_span = -1;
+  for (int k1 = 0; k1 <= c0 / (c1 > 0 ? c1 : 1) + 1; ++k1) {
+    PairSched sc{n0, n1, P, n0 % P, k1};
+    int64_t span = 0;
+    for (int pr = 0; pr < P; ++pr) {
+      int64_t load = 0;
+      const int cnt0 = (n0 - pr + P - 1) / P;
+      load += (int64_t)cnt0 * c0;
+      const int S = P - sc.rem0;
+      for (int i1 = 0;; ++i1) {
+        int j;
+        if (pr >= sc.rem0 && i1 < k1) j = i1 * S + (pr - sc.rem0);
+        else j = S * k1 + (pr >= sc.rem0 ? i1 - k1 : i1) * P + pr;
+        if (j >= n1) break;
+        load += c1;
+      }
+      span = load > span ? load : span;
+    }
+    if (best_span < 0 || span < best_span) {
+      best_span = span;
+      best = sc;
+    }
+  }
+  return best;
+}
+
+template <bool kTwo>
+nvfp4_status launch_pair(const PairProblem& g0, const PairProblem& g1, const PairSched& sc, cudaStream_t s) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(nvfp4_gemm_pair_kernel<kTwo>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPairSmemBytes) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  nvfp4_gemm_pair_kernel<kTwo><<<2 * sc.P, kPairThreads, kPairSmemBytes, s>>>(g0.a, g0.b, g0.sfa, g0.sfb, g0.d, g0.p,
+                                                                               g1, sc);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int pair_tiles(const nvfp4_tensor& a, const nvfp4_tensor& b) { return (int)((a.rows / 256) * (b.rows / kPairBN)); }
+int pair_stages(const nvfp4_tensor& a) { return (int)((a.cols + kKPerStage - 1) / kKPerStage); }
+
+nvfp4_status run_pair(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
+                      float* amax_out, const nvfp4_tensor* yq, cudaStream_t s) {
+  PairProblem g0{}, g1{};
+  const nvfp4_status st = make_pair_problem(g0, a, b, d, d_dtype, ldd, amax_out, yq, g_debug_stall.exchange(0));
+  if (st != NVFP4_OK) return st;
+  const int tiles = pair_tiles(a, b);
+  const int pairs_max = sm_count() / 2;
+  const int P = tiles < pairs_max ? tiles : pairs_max;
+  return launch_pair<false>(g0, g1, PairSched{tiles, 0, P, 0, 0}, s);
+}
+
+// Two BF16-output GEMMs of the same operand format over one tile schedule
+// (the problem with the longer K first, so that the pairs left short by its
+// last round start on the other one).
+nvfp4_status run_pair2(const nvfp4_tensor& a0, const nvfp4_tensor& b0, void* d0, int64_t ldd0,
+                       const nvfp4_tensor& a1, const nvfp4_tensor& b1, void* d1, int64_t ldd1, cudaStream_t s) {
+  const bool swap = a1.cols > a0.cols;
+  const nvfp4_tensor &A0 = swap ? a1 : a0, &B0 = swap ? b1 : b0, &A1 = swap ? a0 : a1, &B1 = swap ? b0 : b1;
+  void* D0 = swap ? d1 : d0;
+  void* D1 = swap ? d0 : d1;
+  const int64_t L0 = swap ? ldd1 : ldd0, L1 = swap ? ldd0 : ldd1;
+  PairProblem g0{}, g1{};
+  nvfp4_status st = make_pair_problem(g0, A0, B0, D0, NVFP4_OUT_BF16, L0, nullptr, nullptr, g_debug_stall.exchange(0));
+  if (st != NVFP4_OK) return st;
+  st = make_pair_problem(g1, A1, B1, D1, NVFP4_OUT_BF16, L1, nullptr, nullptr, 0);
+  if (st != NVFP4_OK) return st;
+  const int n0 = pair_tiles(A0, B0), n1 = pair_tiles(A1, B1);
+  const int pairs_max = sm_count() / 2;
+  const int P = n0 + n1 < pairs_max ? n0 + n1 : pairs_max;
+  return launch_pair<true>(g0, g1, make_sched(n0, pair_stages(A0), n1, pair_stages(A1), P), s);
 }
 
 }  // namespace
 
 void set_gemm_debug_stall(int on) { g_debug_stall.store(on ? 1 : 0); }
+
+nvfp4_status launch_gemm2(const nvfp4_tensor& a0, const nvfp4_tensor& b0, void* d0, int64_t ldd0,
+                          const nvfp4_tensor& a1, const nvfp4_tensor& b1, void* d1, int64_t ldd1, cudaStream_t s) {
+  const bool pair0 = a0.rows % 256 == 0 && b0.rows % 256 == 0, pair1 = a1.rows % 256 == 0 && b1.rows % 256 == 0;
+  if (pair0 && pair1 && a0.format == a1.format) return run_pair2(a0, b0, d0, ldd0, a1, b1, d1, ldd1, s);
+  const nvfp4_status st = launch_gemm(a0, b0, d0, NVFP4_OUT_BF16, ldd0, s);
+  if (st != NVFP4_OK) return st;
+  return launch_gemm(a1, b1, d1, NVFP4_OUT_BF16, ldd1, s);
+}
 
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
                          cudaStream_t s, float* amax_out, const nvfp4_tensor* yq) {

@@ -73,5 +73,10 @@ std::atomic<int>& ring_debug_stall_flag();
 // nullptr (no BF16 store).
 nvfp4_status launch_gemm(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
                          cudaStream_t s, float* amax_out = nullptr, const nvfp4_tensor* yq = nullptr);
+// Two BF16-output GEMMs (d_i = a_i b_i^T) in one launch of the CTA-pair
+// kernel when both take it and share the operand format, so that the second
+// one's tiles fill the first one's last round; otherwise two launches.
+nvfp4_status launch_gemm2(const nvfp4_tensor& a0, const nvfp4_tensor& b0, void* d0, int64_t ldd0,
+                          const nvfp4_tensor& a1, const nvfp4_tensor& b1, void* d1, int64_t ldd1, cudaStream_t s);
 
 }  // namespace nvfp4

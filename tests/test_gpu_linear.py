@@ -67,6 +67,33 @@ def test_layer_step_is_deterministic():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("shape", [(8192, 5120, 20480), (512, 256, 768), (768, 512, 256), (384, 256, 128)])
+def test_bwd_one_launch_equals_separate_gemms(shape):
+    """nvfp4_linear_bwd runs Dgrad and Wgrad as one launch of the CTA-pair
+    kernel over a shared tile schedule when both shapes take that kernel: its
+    dX and dW equal two separate nvfp4_gemm calls on the same quantized
+    operands bit for bit (the last shape, M % 256 != 0, takes two launches)."""
+    M, K, N = shape
+    x, w, dy = workloads.tiny_layer(M=M, K=K, N=N, seed=9)
+    ws = B.linear_workspace(M, K, N)
+    B.nvfp4_linear_fwd(x.cuda(), w.cuda(), 5, ws)
+    dyg = dy.cuda()
+    torch.cuda.synchronize()
+    n0 = B.nvfp4_kernel_launch_count()
+    dx, dw = B.nvfp4_linear_bwd(dyg, K, 5, ws)
+    torch.cuda.synchronize()
+    launches = B.nvfp4_kernel_launch_count() - n0
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    v = B.nvfp4_linear_get_views(ws, M, K, N)
+    dx2 = B.nvfp4_gemm(v["dyq"], v["wtq"])
+    dw2 = B.nvfp4_gemm(v["dytq"], v["xtq"])
+    torch.cuda.synchronize()
+    assert torch.equal(dx, dx2)
+    assert torch.equal(dw, dw2)
+    # amax, the fused quantize, then one GEMM launch (two when M % 256 != 0)
+    assert launches == (3 if M % 256 == 0 else 4)
+
+
 @pytest.mark.parametrize("layer", ["mlp_up", "mlp_down", "qkv"])
 def test_layer_full_size_sampled(layer):
     """The full-size layers: MLP up-projection (M=8192, K=5120, N=20480, the
