@@ -67,7 +67,8 @@ def test_layer_step_is_deterministic():
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("shape", [(8192, 5120, 20480), (512, 256, 768), (768, 512, 256), (384, 256, 128)])
+@pytest.mark.parametrize("shape", [(8192, 5120, 20480), (512, 256, 768), (768, 512, 256), (256, 256, 2048),
+                                   (2048, 256, 256), (256, 1024, 512), (384, 256, 128)])
 def test_bwd_one_launch_equals_separate_gemms(shape):
     """nvfp4_linear_bwd runs Dgrad and Wgrad as one launch of the CTA-pair
     kernel over a shared tile schedule when both shapes take that kernel: its
