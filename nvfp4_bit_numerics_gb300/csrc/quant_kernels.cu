@@ -1,9 +1,10 @@
 // quant_kernels.cu -- the NVFP4 quantization kernels for sm_103a: global
 // amax, 1x16 rowwise quantization (round-to-nearest-even on the TMA tile ring
 // of tile_ring.cuh, stochastic rounding with per-thread loads), the 128x64
-// tile kernel that writes the rowwise and/or the transposed (token-major,
-// Hadamard-transformed) operand from one read, and the 16x16 2D weight
-// quantization (on the tile ring) that writes W and W^T.
+// tile kernels that write the rowwise and/or the transposed (token-major,
+// Hadamard-transformed) operand from one read (round-to-nearest-even on the
+// tile ring, stochastic rounding with register-staged tiles), and the 16x16 2D
+// weight quantization (on the tile ring) that writes W and W^T.
 //
 // Method: "Pretraining Large Language Models with NVFP4" (gist.science
 // summary), Resumo técnico §2 Metodologia: two-level NVFP4 scaling ("Escala
