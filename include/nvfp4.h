@@ -246,6 +246,24 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d_de
                         int64_t ldd, nvfp4_stream stream);
 
 /*
+ * nvfp4_gemm2 -- two independent GEMMs of nvfp4_gemm, d0 = a0 b0^T and
+ * d1 = a1 b1^T (BF16 outputs), in one launch: the layer's Dgrad and Wgrad
+ * (Resumo técnico §2, "Técnicas de Treinamento Integradas", items 2-4, and
+ * §3, "Suporte de Hardware").  When both products take the CTA-pair kernel
+ * (all of a0, b0, a1, b1 with rows % 256 == 0) and share the operand format,
+ * their 256 x 256 tiles run over one persistent tile schedule in which the
+ * CTA pairs that the first product's last round leaves idle start on the
+ * second; each output is bit-identical to its nvfp4_gemm.  Otherwise the two
+ * products are launched one after the other.
+ *   a0, b0, d0_dev, ldd0 and a1, b1, d1_dev, ldd1: as a, b, d_dev, ldd of
+ *            nvfp4_gemm with d_dtype NVFP4_OUT_BF16, each pair checked the same
+ *            way.  d0 and d1 must not overlap.
+ */
+nvfp4_status nvfp4_gemm2(const nvfp4_tensor* a0, const nvfp4_tensor* b0, void* d0_dev, int64_t ldd0,
+                         const nvfp4_tensor* a1, const nvfp4_tensor* b1, void* d1_dev, int64_t ldd1,
+                         nvfp4_stream stream);
+
+/*
  * nvfp4_gemm_amax -- nvfp4_gemm that also yields the amax its output's
  * consumer needs: the global amax that sets the per-tensor scale of the next
  * quantization (Resumo técnico §2, two-level scaling), taken in the epilogue

@@ -47,6 +47,7 @@ EXPORTED = [
     "nvfp4_status_string", "nvfp4_kernel_launch_count", "nvfp4_linear_fwd_noalloc",
     "nvfp4_debug_stall_next_gemm", "nvfp4_gemm_amax", "nvfp4_quantize_mx", "nvfp4_mx_scale_bytes",
     "nvfp4_linear_bf16_fwd", "nvfp4_linear_bf16_bwd", "nvfp4_gemm_quant", "nvfp4_debug_stall_next_quantize",
+    "nvfp4_gemm2",
 ]
 
 
@@ -90,6 +91,7 @@ def load_library(path=LIB_PATH):
         "nvfp4_quantize": (I32, [P, I64, I64, ctypes.POINTER(nvfp4_quant_cfg), T, T, P]),
         "nvfp4_scale_bytes": (SZ, [I64, I64, I32]),
         "nvfp4_gemm": (I32, [T, T, P, I32, I64, P]),
+        "nvfp4_gemm2": (I32, [T, T, P, I64, T, T, P, I64, P]),
         "nvfp4_gemm_amax": (I32, [T, T, P, I32, I64, P, P]),
         "nvfp4_gemm_quant": (I32, [T, T, T, P, I64, P, P]),
         "nvfp4_linear_workspace_bytes": (SZ, [I64, I64, I64]),
@@ -232,6 +234,21 @@ def nvfp4_gemm(a, b, out=None, out_dtype=torch.bfloat16, stream=None):
     _check("nvfp4_gemm", load_library().nvfp4_gemm(ctypes.byref(sa), ctypes.byref(sb), _ptr(out), dt,
                                                    out.stride(0), _stream(stream)))
     return out
+
+
+def nvfp4_gemm2(a0, b0, a1, b1, out0=None, out1=None, stream=None):
+    """(D0, D1) = (ts A0 B0^T, ts A1 B1^T) as BF16, the two GEMMs in one launch
+    when both take the CTA-pair kernel (nvfp4_gemm2 of nvfp4.h)."""
+    dev = a0.codes.device
+    if out0 is None:
+        out0 = torch.empty((a0.rows, b0.rows), dtype=torch.bfloat16, device=dev)
+    if out1 is None:
+        out1 = torch.empty((a1.rows, b1.rows), dtype=torch.bfloat16, device=dev)
+    s0, t0, s1, t1 = a0.struct(), b0.struct(), a1.struct(), b1.struct()
+    _check("nvfp4_gemm2", load_library().nvfp4_gemm2(ctypes.byref(s0), ctypes.byref(t0), _ptr(out0), out0.stride(0),
+                                                     ctypes.byref(s1), ctypes.byref(t1), _ptr(out1), out1.stride(0),
+                                                     _stream(stream)))
+    return out0, out1
 
 
 def nvfp4_gemm_amax(a, b, out=None, out_dtype=torch.bfloat16, amax=None, stream=None):

@@ -284,6 +284,16 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, i
   return launch_gemm(*a, *b, d, d_dtype, ldd, static_cast<cudaStream_t>(stream));
 }
 
+nvfp4_status nvfp4_gemm2(const nvfp4_tensor* a0, const nvfp4_tensor* b0, void* d0, int64_t ldd0,
+                         const nvfp4_tensor* a1, const nvfp4_tensor* b1, void* d1, int64_t ldd1,
+                         nvfp4_stream stream) {
+  nvfp4_status st = check_gemm(a0, b0, d0, NVFP4_OUT_BF16, ldd0);
+  if (st != NVFP4_OK) return st;
+  st = check_gemm(a1, b1, d1, NVFP4_OUT_BF16, ldd1);
+  if (st != NVFP4_OK) return st;
+  return launch_gemm2(*a0, *b0, d0, ldd0, *a1, *b1, d1, ldd1, static_cast<cudaStream_t>(stream));
+}
+
 nvfp4_status nvfp4_gemm_amax(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int32_t d_dtype, int64_t ldd,
                              float* amax_dev, nvfp4_stream stream) {
   if (!amax_dev) return NVFP4_ERR_ARG;

@@ -90,6 +90,27 @@ def test_gemm_argument_checks(lib):
     assert call(_mx(128, 256, layout=0), _mx(256, 256)) == binding.NVFP4_ERR_ARG
 
 
+def test_gemm2_argument_checks(lib):
+    """nvfp4_gemm2 checks each of its two products as nvfp4_gemm does (BF16
+    output), before any launch."""
+    a, b = _t(256, 256), _t(256, 256)
+    d = ctypes.c_void_p(16)
+
+    def call(a0=a, b0=b, d0=d, l0=256, a1=a, b1=b, d1=d, l1=256):
+        return lib.nvfp4_gemm2(ctypes.byref(a0), ctypes.byref(b0), d0, l0, ctypes.byref(a1), ctypes.byref(b1), d1,
+                               l1, None)
+
+    assert lib.nvfp4_gemm2(None, ctypes.byref(b), d, 256, ctypes.byref(a), ctypes.byref(b), d, 256,
+                           None) == binding.NVFP4_ERR_ARG
+    assert call(d0=None) == binding.NVFP4_ERR_ARG
+    assert call(d1=None) == binding.NVFP4_ERR_ARG
+    assert call(a0=_t(100, 256)) == binding.NVFP4_ERR_SHAPE
+    assert call(b1=_t(256, 128)) == binding.NVFP4_ERR_SHAPE
+    assert call(l1=200) == binding.NVFP4_ERR_SHAPE
+    assert call(d1=ctypes.c_void_p(24)) == binding.NVFP4_ERR_ALIGN
+    assert call(a1=_t(256, 256, ts=None)) == binding.NVFP4_ERR_ARG
+
+
 def test_gemm_quant_argument_checks(lib):
     a, b = _t(256, 256), _t(512, 256)
     yq = _t(256, 512, amax=32)

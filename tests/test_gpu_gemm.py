@@ -235,3 +235,29 @@ def test_gemm_sweep_full_size_sampled(K, N, w2d, rht):
         # the transform cancels: the product is close to the unquantized X W^T
         exact = xf[rows].astype(np.float64) @ wf.astype(np.float64).T
         assert rel_fro(got, exact) < 0.15
+
+
+@pytest.mark.parametrize("shapes", [((256, 512, 768), (512, 256, 1024)), ((1024, 256, 512), (256, 512, 256)),
+                                    ((384, 256, 256), (256, 256, 512))])
+def test_gemm2_equals_two_gemms(shapes):
+    """nvfp4_gemm2 gives each product bit-identical to its own nvfp4_gemm, in
+    one launch when all four operands have rows % 256 == 0 (the CTA-pair
+    kernel's two-problem schedule) and in two otherwise (the last case)."""
+    (m0, k0, n0), (m1, k1, n1) = shapes
+    g = torch.Generator().manual_seed(17)
+    ops = []
+    for m, k in ((m0, k0), (n0, k0), (m1, k1), (n1, k1)):
+        x = (torch.randn((m, k), generator=g)).to(torch.bfloat16).cuda()
+        ops.append(B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE, B.NVFP4_ROUND_RNE)[0])
+    a0, b0, a1, b1 = ops
+    torch.cuda.synchronize()
+    n_before = B.nvfp4_kernel_launch_count()
+    d0, d1 = B.nvfp4_gemm2(a0, b0, a1, b1)
+    torch.cuda.synchronize()
+    launches = B.nvfp4_kernel_launch_count() - n_before
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    pair = all(r % 256 == 0 for r in (m0, n0, m1, n1))
+    assert launches == (1 if pair else 2)
+    assert torch.equal(d0, B.nvfp4_gemm(a0, b0))
+    assert torch.equal(d1, B.nvfp4_gemm(a1, b1))
+
