@@ -712,8 +712,8 @@ def run_next(args, rank, world, local):
         "quant_w": lambda: B.nvfp4_quantize_mx(w, both, out=qw, out_t=qwt, stream=stream),
         "quant_dy": lambda: B.nvfp4_quantize_mx(dy, both, out=qdy, out_t=qdyt, stream=stream),
         "gemm_fprop": lambda: B.nvfp4_gemm(qx, qw, out=y, stream=stream),
-        "gemm_dgrad": lambda: B.nvfp4_gemm(qdy, qwt, out=dx, stream=stream),
-        "gemm_wgrad": lambda: B.nvfp4_gemm(qdyt, qxt, out=dw, stream=stream),
+        # Dgrad + Wgrad in one launch, as the NVFP4 layer's backward runs them
+        "gemm_dgrad_wgrad": lambda: B.nvfp4_gemm2(qdy, qwt, qdyt, qxt, out0=dx, out1=dw, stream=stream),
     }
 
     def step():

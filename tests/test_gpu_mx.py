@@ -208,6 +208,33 @@ def test_mx_gemm_amax_and_mixed_formats_rejected():
         B.nvfp4_gemm(qa, nv)
 
 
+def test_mx_gemm2_one_launch():
+    """nvfp4_gemm2 on two MXFP4 products of different K (the Dgrad + Wgrad
+    pattern): one launch, each product bit-identical to its own nvfp4_gemm and
+    within the BF16 tolerance of the oracle's MXFP4 GEMM."""
+    rng = np.random.default_rng(23)
+    shapes = ((512, 768, 256), (256, 512, 1024))  # (M, N, K) of each product
+    ops, refs = [], []
+    for M, N, K in shapes:
+        ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+        bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+        asc = rng.integers(115, 135, size=(M, K // 32)).astype(np.uint8)
+        bsc = rng.integers(115, 135, size=(N, K // 32)).astype(np.uint8)
+        ops += [make_mx(ac, asc), make_mx(bc, bsc)]
+        refs.append(ref_mx(ac, asc, bc, bsc))
+    a0, b0, a1, b1 = ops
+    torch.cuda.synchronize()
+    n_before = B.nvfp4_kernel_launch_count()
+    d0, d1 = B.nvfp4_gemm2(a0, b0, a1, b1)
+    torch.cuda.synchronize()
+    assert B.nvfp4_kernel_launch_count() - n_before == 1
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    assert torch.equal(d0, B.nvfp4_gemm(a0, b0))
+    assert torch.equal(d1, B.nvfp4_gemm(a1, b1))
+    for d, ref in ((d0, refs[0]), (d1, refs[1])):
+        assert rel_fro(d.float().cpu().numpy(), formats.float64_to_bf16_rne(ref)) <= 1e-3
+
+
 def test_mx_full_size_sampled():
     """The MXFP4 layer-shape Fprop (X 8192x5120, W 20480x5120, the 16x
     inter-layer MLP up-projection): sampled rows of the quantized X, its
