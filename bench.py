@@ -203,27 +203,31 @@ def cpu_oracle_step(x_f, w_f, dy_f, threads=0):
     return time.perf_counter() - t0, 6 * ORACLE_TOKENS * K * N
 
 
-def cpu_quantize_full(x_f, w_f, dy_f, threads=0):
+def cpu_quantize_full(x_f, w_f, dy_f, threads=0, tensors=("x", "w", "dy")):
     """The layer step's three quantize passes in full through the plain C++
     oracle: X [8192, 5120] (amax, amax of the transform along tokens, rowwise
     RNE, transposed Hadamard RNE), W [20480, 5120] (amax, 16x16 blocks, W and
     W^T), dY [8192, 20480] (amax, amax of the transform, rowwise SR, transposed
-    Hadamard SR).  Returns {tensor: seconds}."""
+    Hadamard SR).  Returns {tensor: seconds} for the tensors named."""
     from oracle import cxx
 
     out = {}
-    t0 = time.perf_counter()
-    cxx.quantize_1d(x_f, "rne", amax=cxx.tensor_amax(x_f, threads), threads=threads)
-    cxx.quantize_transpose(x_f, "rne", rht_seed=SEED, amax=cxx.amax_rht(x_f, SEED, 0, threads), threads=threads)
-    out["x"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    cxx.quantize_2d(w_f, threads=threads)
-    out["w"] = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    cxx.quantize_1d(dy_f, "sr", seed=SEED, stream_id=0, amax=cxx.tensor_amax(dy_f, threads), threads=threads)
-    cxx.quantize_transpose(dy_f, "sr", seed=SEED, stream_id=1, rht_seed=SEED,
-                           amax=cxx.amax_rht(dy_f, SEED, 0, threads), threads=threads)
-    out["dy"] = time.perf_counter() - t0
+    if "x" in tensors:
+        t0 = time.perf_counter()
+        cxx.quantize_1d(x_f, "rne", amax=cxx.tensor_amax(x_f, threads), threads=threads)
+        cxx.quantize_transpose(x_f, "rne", rht_seed=SEED, amax=cxx.amax_rht(x_f, SEED, 0, threads),
+                               threads=threads)
+        out["x"] = time.perf_counter() - t0
+    if "w" in tensors:
+        t0 = time.perf_counter()
+        cxx.quantize_2d(w_f, threads=threads)
+        out["w"] = time.perf_counter() - t0
+    if "dy" in tensors:
+        t0 = time.perf_counter()
+        cxx.quantize_1d(dy_f, "sr", seed=SEED, stream_id=0, amax=cxx.tensor_amax(dy_f, threads), threads=threads)
+        cxx.quantize_transpose(dy_f, "sr", seed=SEED, stream_id=1, rht_seed=SEED,
+                               amax=cxx.amax_rht(dy_f, SEED, 0, threads), threads=threads)
+        out["dy"] = time.perf_counter() - t0
     return out
 
 
@@ -235,6 +239,9 @@ def cpu_baseline_record(x_f, w_f, dy_f):
     cores = os.cpu_count()
     s, flops = cpu_oracle_step(x_f, w_f, dy_f, threads=cores)
     q = cpu_quantize_full(x_f, w_f, dy_f, threads=cores)
+    # one thread, on X (the 8192x5120 tensor size of the quantize sweep) only,
+    # to keep the run short
+    q1 = cpu_quantize_full(x_f, w_f, dy_f, threads=1, tensors=("x",))
     elems = {"x": M * K, "w": N * K, "dy": M * N}
     # algorithmic bytes: BF16 read once per amax pass and once per quantize
     # pass, 0.5625 B per element per NVFP4 output
@@ -248,6 +255,7 @@ def cpu_baseline_record(x_f, w_f, dy_f):
         "quantize_full": {k: {"s": v, "gbs": qbytes[k] / v / 1e9} for k, v in q.items()},
         "quantize_full_note": "each tensor's amax and quantize passes of the layer step in full "
                               "(X 8192x5120, W 20480x5120, dY 8192x20480)",
+        "quantize_full_1thread": {k: {"s": v, "gbs": qbytes[k] / v / 1e9, "threads": 1} for k, v in q1.items()},
     }
 
 
