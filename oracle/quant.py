@@ -62,7 +62,10 @@ def block_scale_codes(amax_b, s_enc):
     sd = (amax_b / F32(6.0)).astype(np.float32)
     E = formats.e4m3_encode_rne_sat((sd * s_enc).astype(np.float32))
     Ef = formats.e4m3_to_float32(E)
-    with np.errstate(divide="ignore"):
+    # float32 IEEE results throughout: for a tensor whose amax lies near the
+    # bottom of the float range s_enc / E can round to +inf, as a float32
+    # division does (numpy would only warn about it)
+    with np.errstate(divide="ignore", over="ignore"):
         enc = np.where(E == 0, F32(0.0), (s_enc / np.where(E == 0, F32(1.0), Ef)).astype(np.float32))
     return E, enc.astype(np.float32)
 
