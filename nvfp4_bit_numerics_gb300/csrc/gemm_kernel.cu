@@ -1196,9 +1196,15 @@ nvfp4_status make_pair_problem(PairProblem& g, const nvfp4_tensor& a, const nvfp
 // The schedule of n0 tiles of k-length c0 and n1 tiles of k-length c1 over
 // P pairs (pair_tile): the number of head rounds k1 that gives the shortest
 // longest pair, found by counting every pair's stages.
+// The search is linear in the tile count per candidate; a layer calls this
+// with the same shapes every step, so the last answer is kept per thread.
 PairSched make_sched(int n0, int c0, int n1, int c1, int P) {
   PairSched best{n0, n1, P, n1 ? n0 % P : 0, 0};
   if (!n1 || best.rem0 == 0) return best;
+  thread_local int last_key[5] = {-1, -1, -1, -1, -1};
+  thread_local PairSched last{};
+  if (last_key[0] == n0 && last_key[1] == c0 && last_key[2] == n1 && last_key[3] == c1 && last_key[4] == P)
+    return last;
   int64_t best_span = -1;
   for (int k1 = 0; k1 <= c0 / (c1 > 0 ? c1 : 1) + 1; ++k1) {
     PairSched sc{n0, n1, P, n0 % P, k1};
@@ -1222,6 +1228,12 @@ PairSched make_sched(int n0, int c0, int n1, int c1, int P) {
       best = sc;
     }
   }
+  last = best;
+  last_key[0] = n0;
+  last_key[1] = c0;
+  last_key[2] = n1;
+  last_key[3] = c1;
+  last_key[4] = P;
   return best;
 }
 
