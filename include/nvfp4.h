@@ -257,7 +257,8 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d_de
  * products are launched one after the other.
  *   a0, b0, d0_dev, ldd0 and a1, b1, d1_dev, ldd1: as a, b, d_dev, ldd of
  *            nvfp4_gemm with d_dtype NVFP4_OUT_BF16, each pair checked the same
- *            way.  d0 and d1 must not overlap.
+ *            way.  d0 and d1 must not overlap (NVFP4_ERR_ARG if their byte
+ *            ranges intersect).
  */
 nvfp4_status nvfp4_gemm2(const nvfp4_tensor* a0, const nvfp4_tensor* b0, void* d0_dev, int64_t ldd0,
                          const nvfp4_tensor* a1, const nvfp4_tensor* b1, void* d1_dev, int64_t ldd1,

@@ -291,6 +291,12 @@ nvfp4_status nvfp4_gemm2(const nvfp4_tensor* a0, const nvfp4_tensor* b0, void* d
   if (st != NVFP4_OK) return st;
   st = check_gemm(a1, b1, d1, NVFP4_OUT_BF16, ldd1);
   if (st != NVFP4_OK) return st;
+  // the outputs' byte ranges (rows - 1 strides plus one row of BF16) must
+  // not intersect: the two products' tiles run concurrently
+  const uintptr_t p0 = reinterpret_cast<uintptr_t>(d0), p1 = reinterpret_cast<uintptr_t>(d1);
+  const uintptr_t e0 = p0 + (uintptr_t)((a0->rows - 1) * ldd0 + b0->rows) * 2u;
+  const uintptr_t e1 = p1 + (uintptr_t)((a1->rows - 1) * ldd1 + b1->rows) * 2u;
+  if (p0 < e1 && p1 < e0) return NVFP4_ERR_ARG;
   return launch_gemm2(*a0, *b0, d0, ldd0, *a1, *b1, d1, ldd1, static_cast<cudaStream_t>(stream));
 }
 

@@ -109,6 +109,9 @@ def test_gemm2_argument_checks(lib):
     assert call(l1=200) == binding.NVFP4_ERR_SHAPE
     assert call(d1=ctypes.c_void_p(24)) == binding.NVFP4_ERR_ALIGN
     assert call(a1=_t(256, 256, ts=None)) == binding.NVFP4_ERR_ARG
+    # outputs that share bytes: the same buffer, or d1 starting on d0's last row
+    assert call() == binding.NVFP4_ERR_ARG
+    assert call(d1=ctypes.c_void_p(16 + 255 * 256 * 2)) == binding.NVFP4_ERR_ARG
 
 
 def test_gemm_quant_argument_checks(lib):
