@@ -250,9 +250,12 @@ def test_gemm2_equals_two_gemms(shapes):
         x = (torch.randn((m, k), generator=g)).to(torch.bfloat16).cuda()
         ops.append(B.nvfp4_quantize(x, B.NVFP4_Q_ROWWISE, B.NVFP4_ROUND_RNE)[0])
     a0, b0, a1, b1 = ops
+    # outputs pre-filled with NaN: a tile the schedule skipped would show
+    d0 = torch.full((m0, n0), float("nan"), dtype=torch.bfloat16, device="cuda")
+    d1 = torch.full((m1, n1), float("nan"), dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
     n_before = B.nvfp4_kernel_launch_count()
-    d0, d1 = B.nvfp4_gemm2(a0, b0, a1, b1)
+    d0, d1 = B.nvfp4_gemm2(a0, b0, a1, b1, out0=d0, out1=d1)
     torch.cuda.synchronize()
     launches = B.nvfp4_kernel_launch_count() - n_before
     assert B.nvfp4_get_status() == B.NVFP4_OK

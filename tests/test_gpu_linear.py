@@ -79,9 +79,12 @@ def test_bwd_one_launch_equals_separate_gemms(shape):
     ws = B.linear_workspace(M, K, N)
     B.nvfp4_linear_fwd(x.cuda(), w.cuda(), 5, ws)
     dyg = dy.cuda()
+    # outputs pre-filled with NaN: a tile the schedule skipped would show
+    dx = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dw = torch.full((N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
     n0 = B.nvfp4_kernel_launch_count()
-    dx, dw = B.nvfp4_linear_bwd(dyg, K, 5, ws)
+    dx, dw = B.nvfp4_linear_bwd(dyg, K, 5, ws, dx=dx, dw=dw)
     torch.cuda.synchronize()
     launches = B.nvfp4_kernel_launch_count() - n0
     assert B.nvfp4_get_status() == B.NVFP4_OK

@@ -223,9 +223,12 @@ def test_mx_gemm2_one_launch():
         ops += [make_mx(ac, asc), make_mx(bc, bsc)]
         refs.append(ref_mx(ac, asc, bc, bsc))
     a0, b0, a1, b1 = ops
+    # outputs pre-filled with NaN: a tile the schedule skipped would show
+    d0 = torch.full((shapes[0][0], shapes[0][1]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    d1 = torch.full((shapes[1][0], shapes[1][1]), float("nan"), dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
     n_before = B.nvfp4_kernel_launch_count()
-    d0, d1 = B.nvfp4_gemm2(a0, b0, a1, b1)
+    d0, d1 = B.nvfp4_gemm2(a0, b0, a1, b1, out0=d0, out1=d1)
     torch.cuda.synchronize()
     assert B.nvfp4_kernel_launch_count() - n_before == 1
     assert B.nvfp4_get_status() == B.NVFP4_OK
