@@ -31,7 +31,7 @@ namespace {
 
 __device__ uint32_t g_status_word;
 
-uint32_t* g_status_ptr[64] = {nullptr};
+std::atomic<uint32_t*> g_status_ptr[64] = {};
 
 // Random stream ids of one layer step (Philox key = the step's seed).
 constexpr uint32_t kStreamDy = 0;   // stochastic rounding of dY (Dgrad operand)
@@ -77,7 +77,7 @@ std::atomic<int>& ring_debug_stall_flag() {
 }
 
 int device_sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
   if (!cached[dev]) {

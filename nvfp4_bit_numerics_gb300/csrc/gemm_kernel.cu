@@ -1109,7 +1109,7 @@ template <int BN>
 nvfp4_status run(const nvfp4_tensor& a, const nvfp4_tensor& b, void* d, int32_t d_dtype, int64_t ldd,
                  float* amax_out, cudaStream_t s) {
   using C = Cfg<BN>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
@@ -1239,7 +1239,7 @@ PairSched make_sched(int n0, int c0, int n1, int c1, int P) {
 
 template <bool kTwo>
 nvfp4_status launch_pair(const PairProblem& g0, const PairProblem& g1, const PairSched& sc, cudaStream_t s) {
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kRingThreads, kCtasPerSm) mx_quant_kernel(cons
 
 template <bool kRow, bool kT>
 cudaError_t launch(const CUtensorMap& map, const MxParams& p, unsigned grid, cudaStream_t s) {
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {

@@ -800,7 +800,7 @@ cudaError_t launch_rowwise_ring(const void* x, int64_t rows, int64_t cols, const
   CUtensorMap map;
   if (!make_ring_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
   auto kern = quant_rowwise_ring_kernel<kRHT>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
@@ -852,7 +852,7 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
     if (!make_ring_map(&map, x, rows, cols)) return cudaErrorInvalidValue;
     int dev = 0;
     cudaGetDevice(&dev);
-    auto run = [&](auto kern, bool* attr_set) -> cudaError_t {
+    auto run = [&](auto kern, std::atomic<bool>* attr_set) -> cudaError_t {
       if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
@@ -866,7 +866,7 @@ cudaError_t launch_quant_tile(const void* x, int64_t rows, int64_t cols, const n
     };
 #define NVFP4_RING(R, T, H)                                \
   do {                                                     \
-    static bool attr_set[64] = {false};                    \
+    static std::atomic<bool> attr_set[64] = {};           \
     return run(quant_tile_ring_kernel<R, T, H>, attr_set); \
   } while (0)
     if (row && tr) {
@@ -912,7 +912,7 @@ cudaError_t launch_quant_2d(const void* w, int64_t rows, int64_t cols, const nvf
   if (tiles >= kRingMaxTiles) return cudaErrorInvalidValue;
   CUtensorMap map;
   if (!make_ring_map(&map, w, rows, cols)) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
