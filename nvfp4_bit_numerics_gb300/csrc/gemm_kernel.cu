@@ -101,7 +101,7 @@ struct Params {
   int d_f32;
   int M, N, K;
   int sf_tiles_k;  // 4-scale tiles per 128-row scale tile row = K / 64
-  int n_fastest;   // tile order: 1 = consecutive tiles walk N (B stays in L2)
+  int n_fastest;   // tile order: 0 = walk M, 1 = walk N, >= 2 = walk N in groups of that many block rows
   int debug_stall; // failure-detection test: the first stage's loads are never issued
   int tma_store;   // pair kernel: BF16 output written by bulk tensor stores
   uint32_t* amax_out;  // if set: max |D| over the stored output, as float bits (atomicMax)
@@ -118,8 +118,18 @@ struct Params {
 // Tile index -> (m block, n block).  Consecutive tiles (which run at the same
 // time on neighbouring SMs) walk the dimension whose operand is the smaller,
 // so that operand stays resident in L2 while the larger one streams once.
+// n_fastest >= 2 (the walked B operand too large to stay in L2 across waves
+// of tiles): groups of n_fastest block rows, m fastest inside a group, so that
+// the tiles in flight together touch fewer B slabs.
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int n_fastest, int& mb, int& nb) {
-  if (n_fastest) {
+  if (n_fastest >= 2) {
+    const int G = n_fastest, per = G * num_n;
+    const int g = tile / per, idx = tile - g * per;
+    const int m_first = g * G;
+    const int gl = num_m - m_first < G ? num_m - m_first : G;
+    mb = m_first + idx % gl;
+    nb = idx / gl;
+  } else if (n_fastest) {
     nb = tile % num_n;
     mb = tile / num_n;
   } else {
@@ -1175,7 +1185,11 @@ nvfp4_status make_pair_problem(PairProblem& g, const nvfp4_tensor& a, const nvfp
   p.N = (int)b.rows;
   p.K = (int)K;
   p.sf_tiles_k = (int)(K / 64);
-  p.n_fastest = p.N < p.M;
+  // walk N when B is the smaller operand; when its packed codes exceed 32 MB
+  // they do not stay in L2 from one wave of tiles to the next (the Dgrad B,
+  // W^T, at 5120 x 20480: 52 MB), so walk it in groups of 16 block rows
+  // (measured: Dgrad 2.5 % faster; no change where B stays in L2)
+  p.n_fastest = p.N < p.M ? ((int64_t)p.N * p.K / 2 > (int64_t(32) << 20) ? 16 : 1) : 0;
   p.debug_stall = debug_stall;
   p.status = device_status_ptr();
   p.amax_out = reinterpret_cast<uint32_t*>(amax_out);
