@@ -99,10 +99,17 @@ __global__ void __launch_bounds__(kThreads) amax_rht_rows_kernel(const uint4* __
   warp_amax_to_global(mr, out_rht, status);
 }
 
+// NaN-propagating maximum of three floats.
+__device__ __forceinline__ float fmax_nan3(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Plain amax and amax of the 16-point transform along the rows (tokens):
 // one thread per (16-row block, 8-column group); a warp reads 512
 // contiguous bytes of each of the 16 rows.
-__global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(kThreads, 2) amax_rht_cols_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                  int64_t cols, uint64_t seed, uint32_t* out_plain,
                                                                  uint32_t* out_rht, uint32_t* status) {
   const uint32_t smask = rht_sign_mask(seed);
@@ -125,19 +132,35 @@ __global__ void __launch_bounds__(kThreads) amax_rht_cols_kernel(const uint16_t*
       const uint32_t sw = rht_sign_word(smask, i);  // row i of the chunk
       q[i].x ^= sw; q[i].y ^= sw; q[i].z ^= sw; q[i].w ^= sw;
     }
+    // the two columns of each 32-bit word as float pairs through the first
+    // three butterfly stages; the last stage only feeds the maximum:
+    // max(|fl(a + b)|, |fl(a - b)|) = fl(|a| + |b|) (rounding is monotonic)
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float v[16];
+    for (int c2 = 0; c2 < 4; ++c2) {
+      uint64_t pp[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t w = (c < 2) ? q[i].x : (c < 4) ? q[i].y : (c < 6) ? q[i].z : q[i].w;
-        v[i] = (c & 1) ? bf16hi(w) : bf16lo(w);
+      for (int i = 0; i < 16; ++i)
+        pp[i] = f2_from_bf16x2(c2 == 0 ? q[i].x : c2 == 1 ? q[i].y : c2 == 2 ? q[i].z : q[i].w);
+#pragma unroll
+      for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if ((i & h) == 0) {
+            const uint64_t a = pp[i], b = pp[i + h];
+            pp[i] = f2_add(a, b);
+            pp[i + h] = f2_sub(a, b);
+          }
+        }
       }
-      rht16_unsigned(v);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) mr = fmax_nan_abs(mr, v[i]);
+      for (int i = 0; i < 8; ++i) {
+        const uint64_t a = pp[i], b = pp[i + 8];
+        mr = fmax_nan3(mr, __fadd_rn(fabsf(f2_lo(a)), fabsf(f2_lo(b))), __fadd_rn(fabsf(f2_hi(a)), fabsf(f2_hi(b))));
+      }
     }
   }
+  // the transform's * 1/4, applied once: fl(max |v| / 4) = max fl(|v| / 4)
+  mr = __fmul_rn(mr, 0.25f);
   if (out_plain) warp_amax_to_global(max(mp2 & 0xFFFFu, mp2 >> 16) << 16, out_plain, status);
   warp_amax_to_global(__float_as_uint(mr), out_rht, status);
 }
