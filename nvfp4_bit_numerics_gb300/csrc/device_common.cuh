@@ -281,11 +281,11 @@ __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
   return philox4x32_10_seed(u32x4{0u, 0u, kRhtStream, 0u}, (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
 }
 
-// NaN-propagating max of m and |v| (a NaN anywhere makes the result NaN, so
-// it keeps the non-finite detection of a bit-pattern max).
-__device__ __forceinline__ float fmax_nan_abs(float m, float v) {
+// NaN-propagating maximum of three floats (a NaN anywhere makes the result
+// NaN, so it keeps the non-finite detection of a bit-pattern max).
+__device__ __forceinline__ float fmax_nan3(float a, float b, float c) {
   float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(v)));
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 

@@ -99,13 +99,6 @@ __global__ void __launch_bounds__(kThreads) amax_rht_rows_kernel(const uint4* __
   warp_amax_to_global(mr, out_rht, status);
 }
 
-// NaN-propagating maximum of three floats.
-__device__ __forceinline__ float fmax_nan3(float a, float b, float c) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 // Plain amax and amax of the 16-point transform along the rows (tokens):
 // one thread per (16-row block, 8-column group); a warp reads 512
 // contiguous bytes of each of the 16 rows.
