@@ -21,7 +21,7 @@
 // The kernel is bound by HBM bandwidth: 2 bytes read per element, 0.5 + 1/16
 // bytes written per element and output (codes and MMA-layout scale words).
 // It runs on the TMA tile ring of tile_ring.cuh (128 x 64 BF16 tiles in a
-// 4-slot shared-memory ring): threads 0-127 encode one 64-element row chunk
+// 3-slot shared-memory ring): threads 0-127 encode one 64-element row chunk
 // each (rowwise output), threads 128-255 a column pair over 32 rows each
 // (transposed output), so every thread writes whole code runs and scale
 // words while the next tiles are already in flight.

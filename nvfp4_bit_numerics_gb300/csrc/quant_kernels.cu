@@ -492,7 +492,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;
 // one word.  The stochastic-rounding kinds, bound by instruction issue, keep
 // quant_tile_kernel, which runs 24 warps per SM against this kernel's 16.
 // ---------------------------------------------------------------------------
-constexpr int kTileRingCtas = 2;  // CTAs per SM (registers: up to 112 a thread)
+constexpr int kTileRingCtas = 3;  // CTAs per SM: up to 72 registers a thread, 3-slot rings
 
 template <bool kRow, bool kT, bool kRHT>
 __global__ void __launch_bounds__(kRingThreads, kTileRingCtas)

@@ -3,7 +3,7 @@
 // read each tile once and write rowwise and/or transposed outputs from it.
 //
 // One producer warp streams this CTA's tiles (16 KB each, 128-byte swizzle:
-// 16-byte chunk j of row r stored at chunk j ^ (r % 8)) into a 4-slot
+// 16-byte chunk j of row r stored at chunk j ^ (r % 8)) into a 3-slot
 // shared-memory ring with cp.async.bulk.tensor; 8 consumer warps wait for a
 // tile, hand it to the kernel's consumer, and release the slot.  Every wait
 // is bounded (device_async.cuh); on a timeout the consumers stop, the
@@ -28,7 +28,7 @@ constexpr int kRingThreads = 32 * (kRingConsumerWarps + 1);  // + the producer w
 constexpr int kRingTileRows = 128;
 constexpr int kRingTileCols = 64;
 constexpr int kRingTileBytes = kRingTileRows * kRingTileCols * 2;
-constexpr int kRingStages = 4;
+constexpr int kRingStages = 3;
 constexpr int kRingSmemBytes = kRingStages * kRingTileBytes + 1024;  // + alignment of the ring to 1024 B
 constexpr int64_t kRingMaxTiles = int64_t(1) << 31;
 
