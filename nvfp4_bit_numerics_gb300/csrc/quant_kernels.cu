@@ -490,7 +490,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;
 // collected in shared memory (double-buffered) and stored as whole 64-byte
 // row segments and 4-byte scale words; the rowwise scales of a row go out as
 // one word.  The stochastic-rounding kinds, bound by instruction issue, keep
-// quant_tile_kernel, which runs 24 warps per SM against this kernel's 16.
+// quant_tile_kernel: on this ring they ran slower at 2 CTAs per SM (16
+// encoding warps) and at 3 (72 registers, with spills).
 // ---------------------------------------------------------------------------
 constexpr int kTileRingCtas = 3;  // CTAs per SM: up to 72 registers a thread, 3-slot rings
 
