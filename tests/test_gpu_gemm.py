@@ -97,6 +97,31 @@ def test_random_gemm(M, N, K):
     assert rel_fro(d16, ref) <= 4e-3  # BF16 output rounding alone
 
 
+def test_grouped_tile_order_covers_every_tile():
+    """A GEMM whose B codes exceed 32 MB with N < M walks B in groups of 16
+    block rows (20 block rows here: a group of 16 and a partial one of 4).
+    The output, pre-filled with NaN, must be written everywhere, and sampled
+    rows of both groups match the oracle."""
+    M, N, K = 5120, 4096, 18432  # B codes: 4096 x 18432 / 2 = 36 MiB
+    assert N * K // 2 > (32 << 20) and N < M
+    rng = np.random.default_rng(31)
+    ac = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    bc = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    asc = rng.integers(0x28, 0x48, size=(M, K // 16)).astype(np.uint8)
+    bsc = rng.integers(0x28, 0x48, size=(N, K // 16)).astype(np.uint8)
+    ta, tb = 0.05, 0.02
+    qa, qb = make_q(ac, asc, ta), make_q(bc, bsc, tb)
+    d = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.nvfp4_gemm(qa, qb, out=d)
+    torch.cuda.synchronize()
+    assert B.nvfp4_get_status() == B.NVFP4_OK
+    assert not torch.isnan(d).any()
+    rows = np.array([3, 700, 2047, 3000, 4095, 4100, 4700, 5119])  # block rows 0-15 and 16-19
+    ref = ref_gemm(ac[rows], asc[rows], ta, bc, bsc, tb)
+    got = d[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert rel_fro(got, formats.float64_to_bf16_rne(ref)) <= 1e-3
+
+
 def test_strided_output():
     rng = np.random.default_rng(3)
     M, N, K = 128, 256, 256
