@@ -319,9 +319,10 @@ nvfp4_status nvfp4_gemm_quant(const nvfp4_tensor* a, const nvfp4_tensor* b, cons
  *   Dgrad operand); then Y = X W^T (BF16).
  * nvfp4_linear_bwd: amax of dY and of the transformed dY^T; dY -> rowwise SR
  *   (Philox stream 0) and dY^T -> Hadamard + SR (stream 1) in one read; then
- *   dX = dY W and dW = dY^T X (BF16) from the saved operands.  The Hadamard
- *   signs come from `seed` (stream 2) and must be the same seed as fwd's, so
- *   the transform cancels in dW.
+ *   dX = dY W and dW = dY^T X (BF16) from the saved operands, both in one
+ *   GEMM launch when M, K and N are multiples of 256 (as nvfp4_gemm2).  The
+ *   Hadamard signs come from `seed` (stream 2) and must be the same seed as
+ *   fwd's, so the transform cancels in dW.
  *   x_dev, w_dev, dy_dev, y_dev, dx_dev, dw_dev: BF16 row-major.
  *   ws_dev   workspace of nvfp4_linear_workspace_bytes(M, K, N) bytes; fwd
  *            writes the saved operands there and bwd reads them, so the same
